@@ -1,0 +1,64 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each case edits one line of a copy of the oracle's C source (a dropped term, a
+wrong sign, a slipped index, a transposed operand, a wrong tie rule ...),
+compiles it to a temporary library and runs the pin suite against it in a
+subprocess.  The suite has to go red for every mutant.  The real oracle source
+is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "gate_up_swapped": ("h[i] = orc_silu(g[i]) * u[i];", "h[i] = orc_silu(u[i]) * g[i];"),
+    "row_scale_index": ("wrow[cc] = (double)s[r] * (double)q[(size_t)r * cols + cc];",
+                        "wrow[cc] = (double)s[cc % rows] * (double)q[(size_t)r * cols + cc];"),
+    "weight_transposed": ("wrow[cc] = (double)s[r] * (double)q[(size_t)r * cols + cc];",
+                          "wrow[cc] = (double)s[r] * (double)q[((size_t)cc * rows + r) % ((size_t)rows * cols)];"),
+    "no_renorm": ("if (c->norm_topk) v = v / wsum;", "if (c->norm_topk) v = v;"),
+    "weights_from_corrected": ("      wsrc[e] = s;\n", "      wsrc[e] = s + (bias ? (double)bias[e] : 0.0);\n"),
+    "group_score_top1": ("gscore[g] = sel_score[msorted[0]] + (gs > 1 ? sel_score[msorted[1]] : 0.0);",
+                         "gscore[g] = sel_score[msorted[0]];"),
+    "ties_to_higher": ("if (best < 0 || score[cand[i]] > score[cand[best]]) best = i;",
+                       "if (best < 0 || score[cand[i]] >= score[cand[best]]) best = i;"),
+    "perm_slot_major": ("    for (int t = 0; t < T; t++)\n      for (int j = 0; j < k; j++)\n        if (ids[t * k + j] == e)",
+                        "    for (int j = 0; j < k; j++)\n      for (int t = 0; t < T; t++)\n        if (ids[t * k + j] == e)"),
+    "shared_dropped": ("if (c->n_shared) orc_expert_forward(c, shared, x, T, out);",
+                       "if (0) orc_expert_forward(c, shared, x, T, out);"),
+    "combine_weight_dropped": ("out[(size_t)t * H + h] += w[t * k + j] * yslot",
+                               "out[(size_t)t * H + h] += yslot"),
+    "q8_round_half_even": ("float rr = roundf(r);", "float rr = rintf(r);"),
+    "q8_scale_255": ("volatile float db = amax / 127.0f;", "volatile float db = amax / 128.0f;"),
+    "int4_no_sign_ext": ("q[i] = sext(p[i / 2] >> 4, 4);", "q[i] = (int8_t)(p[i / 2] >> 4);"),
+    "int4_nibble_order": ("out[i / 2] = (uint8_t)(((q[i] & 0xF) << 4) | (q[i + 1] & 0xF));",
+                          "out[i / 2] = (uint8_t)(((q[i + 1] & 0xF) << 4) | (q[i] & 0xF));"),
+    "logit_index": ("acc += x[(size_t)t * H + h] * (double)wr[(size_t)e * H + h];",
+                    "acc += x[(size_t)t * H + h] * (double)wr[((size_t)h * E + e) % ((size_t)E * H)];"),
+    "sigmoid_sign": ("double s = 1.0 / (1.0 + exp(-l[e]));", "double s = 1.0 / (1.0 + exp(l[e]));"),
+    "block_dot_offset": ("acc += (int32_t)a[i] * (int32_t)b[i];", "acc += (int32_t)a[i] * (int32_t)b[31 - i];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    msrc = tmp_path / "moe_oracle.c"
+    msrc.write_text(src.replace(old, new))
+    so = str(tmp_path / "libmut.so")
+    oracle.build(force=True, src=str(msrc), out=so)
+    env = dict(os.environ, MOE_ORACLE_SO=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
