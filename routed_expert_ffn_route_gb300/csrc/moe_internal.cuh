@@ -1,0 +1,174 @@
+// moe_internal.cuh -- private layouts and helpers of the GB300 MoE-layer library.
+//
+// Packed weight blob (device memory, caller-owned; private layout, versioned header):
+//   [header 256 B][router_w fp32 E*H][router_bias fp32 E][expert 0]...[expert E-1][shared]
+// Every expert block is 4096-byte aligned and holds
+//   gate/up codes : (I/64 m-tiles) x (H/64 k-chunks) blocks of [128 rows][CB bytes]
+//                   rows interleaved: row 2j = gate row (64*mt + j), row 2j+1 = up row
+//   down codes    : (H/128 m-tiles) x (I/64 k-chunks) blocks of [128 rows][CB bytes]
+//   gate/up scales: fp32 [I/64][128], same interleave as the rows
+//   down scales   : fp32 [H]
+// CB = 64 * bits / 8 bytes: one row's 64 contraction elements of one k-chunk.
+// Code order inside a row chunk (biased codes, b = q + 2^(bits-1)):
+//   int4: 8 words of 32 bits; word w holds elements 8w..8w+7, element 8w+2p+s in
+//         nibble p+4s  (so (word >> 4p) & 0x000F000F yields the pair (2p, 2p+1)).
+//   int2: 4 words; word w holds elements 16w..16w+15, element 16w+2p+s in 2-bit
+//         field p+8s  (so (word >> 2p) & 0x00030003 yields the pair (2p, 2p+1)).
+//   int8: 16 words; element 4w+i in byte i of word w, plain two's complement.
+// The [128 rows][CB] blocks stream as contiguous 4 KB (int4) units; a row's pair
+// layout feeds both the fp32 FMA path and a 16-bit tensor-core operand directly.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr uint32_t kMagic = 0x50454F4Du;  // "MOEP"
+constexpr uint32_t kVersion = 1;
+constexpr int kHeaderBytes = 256;
+constexpr int kKChunk = 64;     // contraction elements per chunk
+constexpr int kTileRows = 128;  // weight rows per block
+
+struct PackHeader {
+  uint32_t magic, version;
+  int32_t hidden, inter, inter_shared, n_experts, n_shared, weight_bits;
+  int32_t act_q8_0, router, n_group, topk_group;
+};
+
+struct ExpertLayout {
+  int inter;                 // I of this expert
+  uint64_t gu_off, down_off, sgu_off, sd_off;  // relative to the expert base
+  uint64_t bytes;            // stride of the expert block (aligned)
+};
+
+struct PackLayout {
+  uint64_t router_w_off, router_b_off, experts_off, shared_off, total;
+  ExpertLayout routed, shared;
+};
+
+static inline uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+static inline ExpertLayout expert_layout(int H, int I, int bits) {
+  ExpertLayout L;
+  L.inter = I;
+  uint64_t cb = (uint64_t)kKChunk * bits / 8;
+  uint64_t gu = (uint64_t)(I / 64) * (H / kKChunk) * kTileRows * cb;
+  uint64_t dn = (uint64_t)(H / kTileRows) * (I / kKChunk) * kTileRows * cb;
+  L.gu_off = 0;
+  L.down_off = align_up(gu, 256);
+  L.sgu_off = align_up(L.down_off + dn, 256);
+  L.sd_off = align_up(L.sgu_off + (uint64_t)2 * I * 4, 256);
+  L.bytes = align_up(L.sd_off + (uint64_t)H * 4, 4096);
+  return L;
+}
+
+static inline PackLayout pack_layout(const moe_layer_config &c) {
+  PackLayout P;
+  int Is = c.inter_shared ? c.inter_shared : c.inter;
+  P.router_w_off = kHeaderBytes;
+  P.router_b_off = align_up(P.router_w_off + (uint64_t)c.n_experts * c.hidden * 4, 256);
+  P.experts_off = align_up(P.router_b_off + (uint64_t)c.n_experts * 4, 4096);
+  P.routed = expert_layout(c.hidden, c.inter, c.weight_bits);
+  P.shared = expert_layout(c.hidden, Is, c.weight_bits);
+  P.shared_off = P.experts_off + P.routed.bytes * (uint64_t)c.n_experts;
+  P.total = P.shared_off + (c.n_shared ? P.shared.bytes : 0);
+  return P;
+}
+
+// ---------------------------------------------------------------- workspace
+// [ctrl 256 B][router partials fp32 HS*T*E][offsets E+1][perm T*k][slot_pos T*k]
+// [groups int4 max_groups][xq int8 T*H][xd fp32 T*H/32][h fp32 R*Imax][y fp32 R*H]
+// with R = T*k + n_shared*T rows (routed slots in permuted order, then shared tokens).
+struct Ctrl {
+  int status;      // moe_status recorded on the device (0 = OK)
+  int detail;      // where it was recorded (kernel id)
+  int n_groups;    // routed groups written by the permute kernel
+  int pad[61];
+};
+
+constexpr int kRouterHS = 8;  // H splits of the small-T router GEMV
+
+struct WsLayout {
+  uint64_t ctrl, partials, offsets, perm, slot_pos, groups, xq, xd, h, y, total;
+  int max_groups, group_n, rows;
+};
+
+int choose_group_n(const moe_layer_config &c, int T);
+size_t permute_smem(int T, int E);
+
+static inline WsLayout ws_layout(const moe_layer_config &c, int T) {
+  WsLayout W;
+  int Is = c.inter_shared ? c.inter_shared : c.inter;
+  int Imax = c.inter > Is ? c.inter : Is;
+  int k = c.top_k;
+  W.group_n = choose_group_n(c, T);
+  W.rows = T * k + (c.n_shared ? T : 0);
+  int tk = T * k;
+  W.max_groups = (tk + W.group_n - 1) / W.group_n + (c.n_experts < tk ? c.n_experts : tk) +
+                 (c.n_shared ? (T + W.group_n - 1) / W.group_n : 0) + 1;
+  uint64_t o = 0;
+  W.ctrl = o; o += 256;
+  W.partials = o; o = align_up(o + (uint64_t)kRouterHS * T * c.n_experts * 4, 256);
+  W.offsets = o; o = align_up(o + (uint64_t)(c.n_experts + 1) * 4, 256);
+  W.perm = o; o = align_up(o + (uint64_t)tk * 4, 256);
+  W.slot_pos = o; o = align_up(o + (uint64_t)tk * 4, 256);
+  W.groups = o; o = align_up(o + (uint64_t)W.max_groups * 16, 256);
+  W.xq = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * c.hidden : 0), 256);
+  W.xd = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * (c.hidden / 32) * 4 : 0), 256);
+  W.h = o; o = align_up(o + (uint64_t)W.rows * Imax * 4, 256);
+  W.y = o; o = align_up(o + (uint64_t)W.rows * c.hidden * 4, 256);
+  W.total = o;
+  return W;
+}
+
+// ---------------------------------------------------------------- device helpers
+enum KernelId { kKRouter = 1, kKTopk = 2, kKPermute = 3, kKGateUp = 4, kKDown = 5,
+                kKCombine = 6, kKQuant = 7, kKDebugWait = 8 };
+
+__device__ __forceinline__ void record_status(Ctrl *ctrl, int status, int where) {
+  if (atomicCAS(&ctrl->status, 0, status) == 0) ctrl->detail = where;
+}
+
+// A routed group: `n` permuted rows starting at `pos0` that all use expert `e`.
+// For the shared expert (e == E), rows are tokens pos0 .. pos0+n-1.
+struct Group {
+  int e, pos0, n, pad;
+};
+
+// ---------------------------------------------------------------- launch helpers
+struct DevInfo {
+  int sms;
+  int smem_optin;
+};
+DevInfo dev_info();
+
+// kernels (one translation unit each)
+int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *x, moe_dtype dt,
+                  int T, int32_t *ids, float *w, uint8_t *ws, const WsLayout &W,
+                  cudaStream_t st);
+int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t *ws,
+                   const WsLayout &W, cudaStream_t st);
+int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T, uint8_t *ws,
+                   const WsLayout &W, cudaStream_t st);
+int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
+                   moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st);
+int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
+                   const WsLayout &W, cudaStream_t st);
+int launch_pack_expert(const moe_layer_config &c, const ExpertLayout &L, const int8_t *gate,
+                       const int8_t *up, const int8_t *down, const float *sg, const float *su,
+                       const float *sd, uint8_t *base, cudaStream_t st);
+int launch_unpack_expert(const moe_layer_config &c, const ExpertLayout &L, const uint8_t *base,
+                         int8_t *gate, int8_t *up, int8_t *down, float *sg, float *su, float *sd,
+                         cudaStream_t st);
+int launch_write_header(const moe_layer_config &c, uint8_t *packed, cudaStream_t st);
+int launch_q8_quantize(const void *x, moe_dtype dt, int T, int n, int8_t *q, float *d,
+                       cudaStream_t st);
+int launch_block_dots(const moe_layer_config &c, const uint8_t *mat, int K, int mat_rows,
+                      int which, const int32_t *rows, int n_rows, const int8_t *qa, int n_tok,
+                      int32_t *dots, cudaStream_t st);
+int launch_debug_wait(uint8_t *ws, int iterations, cudaStream_t st);
+
+}  // namespace moe

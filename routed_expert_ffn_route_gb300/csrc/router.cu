@@ -1,0 +1,293 @@
+// router.cu -- router logits and top-k selection.
+//
+// Logits: logits[t][e] = sum_h x[t][h] * Wr[e][h] in fp32 ("Colibri——面向前沿大模型推理的轻量级
+// MoE引擎", §3.2 Step 1 gate projection; "colibrì 深度拆解", §4.3 router_forward).
+//  - T <= 16: a GEMV split over (8 experts) x (H/8 slices) per CTA so that all SMs stream the
+//    fp32 router matrix at once; the 8 partial sums are added in a fixed order afterwards.
+//  - T > 16: a tiled CUDA-core GEMM (64 tokens x 64 experts per CTA).
+// Selection, one warp per token:
+//  - softmax router: softmax with the maximum subtracted, the k largest, renormalised
+//    (§3.2 Steps 2-3 of the same page);
+//  - sigmoid grouped router ("Show HN: 如何在我的低配置电脑上运行 GLM-5.2", 已实现的功能:
+//    DeepSeek-V3 风格 sigmoid 路由器 noaux_tc, routed_scaling_factor): s = sigmoid(logit),
+//    c = s + bias; group score = sum of the two largest c of the group; the topk_group best
+//    groups are kept; the k largest c of the kept groups are selected; weights are
+//    s / sum(selected s) * routed_scaling_factor.
+// Ties go to the lower index everywhere; slots are in descending selection score.
+#include "dev.cuh"
+#include "moe_internal.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ void check_header(const uint8_t *packed, const moe_layer_config &c,
+                                             Ctrl *ctrl) {
+  const PackHeader *h = (const PackHeader *)packed;
+  int Is = c.inter_shared ? c.inter_shared : c.inter;
+  if (h->magic != kMagic || h->version != kVersion || h->hidden != c.hidden ||
+      h->inter != c.inter || h->inter_shared != Is || h->n_experts != c.n_experts ||
+      h->n_shared != c.n_shared || h->weight_bits != c.weight_bits)
+    record_status(ctrl, MOE_ERR_PACKED, kKRouter);
+}
+
+template <int TM>
+__global__ void __launch_bounds__(256) router_gemv_kernel(moe_layer_config c, const uint8_t *packed,
+                                                          const float *wr, const void *x,
+                                                          int is_bf16, int T, float *partials,
+                                                          Ctrl *ctrl) {
+  extern __shared__ float xs[];  // [T][HL]
+  const int H = c.hidden, E = c.n_experts;
+  const int HL = H / kRouterHS;
+  const int hs = blockIdx.y;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_header(packed, c, ctrl);
+  for (int i = threadIdx.x; i < T * HL; i += blockDim.x) {
+    int t = i / HL, cc = i % HL;
+    long src = (long)t * H + (long)hs * HL + cc;
+    xs[i] = is_bf16 ? bf16_to_f32(((const uint16_t *)x)[src]) : ((const float *)x)[src];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + warp;
+  if (e >= E) return;
+  const float4 *wrow = (const float4 *)(wr + (long)e * H + (long)hs * HL);
+  float acc[TM];
+#pragma unroll
+  for (int t = 0; t < TM; t++) acc[t] = 0.f;
+  for (int q = lane; q < HL / 4; q += 32) {
+    float4 wv = __ldg(wrow + q);
+#pragma unroll
+    for (int t = 0; t < TM; t++) {
+      if (t < T) {
+        float4 xv = *(const float4 *)(xs + t * HL + 4 * q);
+        acc[t] = fmaf(wv.x, xv.x, acc[t]);
+        acc[t] = fmaf(wv.y, xv.y, acc[t]);
+        acc[t] = fmaf(wv.z, xv.z, acc[t]);
+        acc[t] = fmaf(wv.w, xv.w, acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TM; t++) {
+    if (t < T) {
+      float s = warp_sum(acc[t]);
+      if (lane == 0) partials[((long)hs * T + t) * E + e] = s;
+    }
+  }
+}
+
+// Tiled fp32 GEMM: partials[0][t][e] = sum_h x[t][h] Wr[e][h]; 64x64 tile, 4x4 per thread.
+__global__ void __launch_bounds__(256) router_gemm_kernel(moe_layer_config c, const uint8_t *packed,
+                                                          const float *wr, const void *x,
+                                                          int is_bf16, int T, float *partials,
+                                                          Ctrl *ctrl) {
+  __shared__ float As[32][64 + 4];  // [k][token]
+  __shared__ float Bs[32][64 + 4];  // [k][expert]
+  const int H = c.hidden, E = c.n_experts;
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_header(packed, c, ctrl);
+  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < H; k0 += 32) {
+    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
+      int r = i / 32, kk = i % 32;
+      int t = t0 + r, e = e0 + r;
+      float xv = 0.f, wv = 0.f;
+      if (t < T) {
+        long src = (long)t * H + k0 + kk;
+        xv = is_bf16 ? bf16_to_f32(((const uint16_t *)x)[src]) : ((const float *)x)[src];
+      }
+      if (e < E) wv = __ldg(wr + (long)e * H + k0 + kk);
+      As[kk][r] = xv;
+      Bs[kk][r] = wv;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < 32; kk++) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; i++) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      int e = e0 + tx * 4 + j;
+      if (e < E) partials[(long)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+struct Cand {
+  float s;  // selection score
+  int e;    // expert index (large = none)
+  float w;  // weight source value
+};
+
+__device__ __forceinline__ bool better(const Cand &a, const Cand &b) {
+  return a.s > b.s || (a.s == b.s && a.e < b.e);
+}
+
+__device__ __forceinline__ Cand warp_best(Cand c) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    Cand d;
+    d.s = __shfl_xor_sync(0xffffffffu, c.s, o);
+    d.e = __shfl_xor_sync(0xffffffffu, c.e, o);
+    d.w = __shfl_xor_sync(0xffffffffu, c.w, o);
+    if (better(d, c)) c = d;
+  }
+  return c;
+}
+
+constexpr int kMaxV = 8;  // experts per lane (E <= 256)
+
+__global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, const float *bias,
+                                                          const float *partials, int hsplits,
+                                                          int T, int32_t *ids, float *w,
+                                                          Ctrl *ctrl) {
+  __shared__ float csm[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const int E = c.n_experts, k = c.top_k;
+  const bool grouped = c.router == MOE_ROUTER_SIGMOID_GROUPED;
+  float sel[kMaxV], wsrc[kMaxV];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int v = 0; v < kMaxV; v++) {
+    int e = lane + 32 * v;
+    float l = -INFINITY;
+    if (e < E) {
+      l = 0.f;
+      for (int hs = 0; hs < hsplits; hs++) l += partials[((long)hs * T + t) * E + e];
+      if (!isfinite(l)) {
+        // a non-finite logit: report it, and keep the selection total and in range
+        record_status(ctrl, MOE_ERR_NUMERIC, kKTopk);
+        l = -INFINITY;
+      }
+    }
+    sel[v] = l;
+    mx = fmaxf(mx, l);
+  }
+  float sum_all = 1.f;
+  if (!grouped) {
+    mx = warp_max(mx);
+    float s = 0.f;
+#pragma unroll
+    for (int v = 0; v < kMaxV; v++) {
+      int e = lane + 32 * v;
+      wsrc[v] = e < E ? expf(sel[v] - mx) : 0.f;
+      s += wsrc[v];
+    }
+    sum_all = warp_sum(s);
+  } else {
+#pragma unroll
+    for (int v = 0; v < kMaxV; v++) {
+      int e = lane + 32 * v;
+      if (e < E) {
+        float sg = 1.0f / (1.0f + expf(-sel[v]));
+        wsrc[v] = sg;
+        sel[v] = sg + bias[e];
+        if (isnan(sel[v])) sel[v] = -INFINITY;
+        csm[warp][e] = sel[v];
+      } else {
+        wsrc[v] = 0.f;
+      }
+    }
+  }
+  unsigned allowed_groups = 0xffffffffu;
+  int gs = E;
+  if (grouped) {
+    __syncwarp();
+    const int G = c.n_group;
+    gs = E / G;
+    Cand gc{-INFINITY, 1 << 30, 0.f};
+    if (lane < G) {
+      float b1 = -INFINITY, b2 = -INFINITY;
+      for (int i = 0; i < gs; i++) {
+        float v = csm[warp][lane * gs + i];
+        if (v > b1) { b2 = b1; b1 = v; }
+        else if (v > b2) { b2 = v; }
+      }
+      gc.s = gs > 1 ? b1 + b2 : b1;
+      gc.e = lane;
+    }
+    allowed_groups = 0;
+    for (int j = 0; j < c.topk_group; j++) {
+      Cand b = warp_best(gc);
+      allowed_groups |= 1u << b.e;
+      if (lane == b.e) gc.s = -INFINITY, gc.e = 1 << 30;
+    }
+  }
+  unsigned taken = 0;
+  float my_w = 0.f, wsum = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; j++) {
+    Cand best{-INFINITY, 1 << 30, 0.f};
+#pragma unroll
+    for (int v = 0; v < kMaxV; v++) {
+      int e = lane + 32 * v;
+      bool ok = e < E && !((taken >> v) & 1) && ((allowed_groups >> (e / gs)) & 1);
+      if (ok) {
+        Cand cd{sel[v], e, wsrc[v]};
+        if (better(cd, best)) best = cd;
+      }
+    }
+    Cand b = warp_best(best);
+    if ((b.e & 31) == lane && b.e < E) taken |= 1u << (b.e >> 5);
+    wsum += b.w;
+    if (lane == j) { my_id = b.e; my_w = b.w; }
+  }
+  if (lane < k) {
+    float v;
+    if (c.norm_topk) v = my_w / wsum;
+    else v = grouped ? my_w : my_w / sum_all;
+    ids[(long)t * k + lane] = my_id;
+    w[(long)t * k + lane] = v * c.routed_scaling_factor;
+  }
+}
+
+int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *x, moe_dtype dt,
+                  int T, int32_t *ids, float *w, uint8_t *ws, const WsLayout &W,
+                  cudaStream_t st) {
+  const PackLayout P = pack_layout(c);
+  const float *wr = (const float *)(packed + P.router_w_off);
+  float *partials = (float *)(ws + W.partials);
+  Ctrl *ctrl = (Ctrl *)(ws + W.ctrl);
+  int is_bf16 = dt == MOE_DT_BF16;
+  int hsplits;
+  if (T <= 16 && (size_t)T * (c.hidden / kRouterHS) * 4 <= 96 * 1024) {
+    hsplits = kRouterHS;
+    dim3 grid((c.n_experts + 7) / 8, kRouterHS);
+    size_t smem = (size_t)T * (c.hidden / kRouterHS) * 4;
+    if (smem > 48 * 1024) {
+      cudaFuncSetAttribute(router_gemv_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+      cudaFuncSetAttribute(router_gemv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+    }
+#define GEMV(TM) router_gemv_kernel<TM><<<grid, 256, smem, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl)
+    if (T <= 1) GEMV(1);
+    else if (T <= 2) GEMV(2);
+    else if (T <= 4) GEMV(4);
+    else if (T <= 8) GEMV(8);
+    else GEMV(16);
+#undef GEMV
+  } else {
+    hsplits = 1;
+    dim3 grid((c.n_experts + 63) / 64, (T + 63) / 64);
+    router_gemm_kernel<<<grid, 256, 0, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl);
+  }
+  const float *bias = (const float *)(packed + P.router_b_off);
+  router_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(c, bias, partials, hsplits, T, ids, w, ctrl);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

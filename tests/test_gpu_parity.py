@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 CPU oracle.
+
+Bit-exact: expert ids (slot order included), the permutation, packing round trips,
+Q8_0 codes and int32 block dots.  Floating point (layer output, routed weights):
+max|err| <= 2e-3 * RMS(oracle) and ||err||_F <= 1e-3 * ||oracle||_F.
+Inputs are seeded and margin-filtered (every routing decision has a score gap of at
+least 1e-4); the number of redraws is printed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import gen.device
+import oracle
+import routed_expert_ffn_route_gb300 as moe
+from _gpu_support import GpuLayer, get_layer, inputs, oracle_out
+from _support import FROB_REL, MAX_REL_RMS, err_stats
+
+pytestmark = pytest.mark.gpu
+
+
+def small(name="grouped", **kw):
+    """Several m-tiles, a ragged token tail and both routers at small sizes."""
+    if name == "grouped":
+        base = dict(name="small_grouped", hidden=512, inter=384, n_experts=16, top_k=4,
+                    router="sigmoid_grouped", n_shared=1, inter_shared=256, n_group=4,
+                    topk_group=2, rsf=2.5, bias_std=0.1)
+    else:
+        base = dict(name="small_softmax", hidden=384, inter=256, n_experts=8, top_k=2,
+                    router="softmax")
+    base.update(kw)
+    return gen.LayerSpec(**base)
+
+
+def assert_close(got, ref, what):
+    mx, fr = err_stats(got, ref)
+    print(f"{what}: max|err|/RMS = {mx:.2e}, rel Frobenius = {fr:.2e}")
+    assert mx <= MAX_REL_RMS and fr <= FROB_REL, (what, mx, fr)
+
+
+def check_layer(spec, T, batch=0, sample=None, seed=0):
+    L = get_layer(spec, seed)
+    x, xd, ids_o, w_o, margin, redraws = inputs(spec, L, batch, T)
+    out, ids, w = L.forward(xd)
+    torch.cuda.synchronize()
+    ids_g, w_g, out_g = ids.cpu().numpy(), w.cpu().numpy(), out.cpu().numpy()
+    print(f"{spec.name} T={T}: {redraws} near-tie redraws")
+    assert np.array_equal(ids_g, ids_o), "expert ids differ from the oracle"
+    assert_close(w_g, w_o, f"{spec.name} T={T} weights")
+    off_o, perm_o = oracle.permutation(ids_o, spec.n_experts)
+    off_g, perm_g = L.permutation(T)
+    assert np.array_equal(off_g, off_o) and np.array_equal(perm_g, perm_o)
+    tok = None if sample is None else np.unique(
+        np.linspace(0, T - 1, sample).round().astype(int))
+    ref = oracle_out(spec, L, x, ids_o, w_o, tok)
+    got = out_g if tok is None else out_g[tok]
+    assert_close(got, ref, f"{spec.name} T={T} output")
+    return out, ids, w, xd, L
+
+
+# ------------------------------------------------------------------ packing
+
+@pytest.mark.parametrize("bits", [4, 8, 2])
+def test_pack_unpack_bit_identity(bits):
+    s = small("grouped", weight_bits=bits)
+    L = GpuLayer(s, seed=3)
+    for e in (0, 7, s.n_experts):
+        rows = {w: gen.expert_rows_cols(s, w, shared=(e == s.n_experts)) for w in ("gate", "up", "down")}
+        outs = {w: torch.empty(rows[w], dtype=torch.int8, device="cuda") for w in rows}
+        sc = {w: torch.empty(rows[w][0], dtype=torch.float32, device="cuda") for w in rows}
+        moe.moe_unpack_weights(L.cfg, L.packed, e, outs["gate"], outs["up"], outs["down"],
+                               sc["gate"], sc["up"], sc["down"])
+        torch.cuda.synchronize()
+        for w in rows:
+            assert np.array_equal(outs[w].cpu().numpy(), gen.expert_codes(s, 3, 0, e, w))
+            assert np.array_equal(sc[w].cpu().numpy(), gen.expert_scales(s, 3, 0, e, w))
+
+
+def test_pack_unpack_full_size_expert():
+    s = gen.spec("dsv3")
+    L = get_layer(s)
+    for e in (5, 256):
+        g = torch.empty((2048, 6144), dtype=torch.int8, device="cuda")
+        d = torch.empty((6144, 2048), dtype=torch.int8, device="cuda")
+        moe.moe_unpack_weights(L.cfg, L.packed, e, g, None, d)
+        ref_g = gen.expert_codes_torch(s, 0, 0, e, "gate", "cuda")
+        ref_d = gen.expert_codes_torch(s, 0, 0, e, "down", "cuda")
+        assert torch.equal(g, ref_g) and torch.equal(d, ref_d)
+
+
+# ------------------------------------------------------------------ router
+
+@pytest.mark.parametrize("name,T", [("tiny", 8), ("tiny", 1), ("mixtral", 1), ("mixtral", 512),
+                                    ("dsv3", 1), ("dsv3", 16), ("dsv3", 2048)])
+def test_router_parity(name, T):
+    s = gen.spec(name)
+    L = get_layer(s)
+    x, xd, ids_o, w_o, margin, redraws = inputs(s, L, 1, T)
+    ids, w = L.route(xd)
+    torch.cuda.synchronize()
+    print(f"{name} T={T}: {redraws} near-tie redraws")
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert_close(w.cpu().numpy(), w_o, f"router {name} T={T} weights")
+    if s.router == "sigmoid_grouped":
+        assert np.allclose(w.cpu().numpy().sum(1), s.rsf, rtol=1e-5)
+
+
+@pytest.mark.parametrize("kw", [dict(n_experts=1, top_k=1), dict(top_k=8),
+                                dict(norm_topk=0)])
+def test_router_softmax_special_cases(kw):
+    s = small("softmax", **kw)
+    check_layer(s, 5, seed=4)
+
+
+@pytest.mark.parametrize("kw", [dict(n_group=1, topk_group=1), dict(topk_group=4),
+                                dict(rsf=1.0, bias_std=0.0), dict(top_k=8, topk_group=2)])
+def test_router_grouped_special_cases(kw):
+    s = small("grouped", **kw)
+    check_layer(s, 6, seed=5)
+
+
+# ------------------------------------------------------------------ whole layer
+
+def test_layer_tiny_full():
+    check_layer(gen.spec("tiny"), 8)
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 33, 37, 64])
+def test_layer_small_grouped_ragged(T):
+    check_layer(small("grouped"), T, seed=1)
+
+
+@pytest.mark.parametrize("bits", [8, 2])
+def test_layer_small_other_bit_widths(bits):
+    check_layer(small("grouped", weight_bits=bits), 19, seed=2)
+
+
+@pytest.mark.parametrize("T", [3, 40])
+def test_layer_small_q8_0(T):
+    check_layer(small("grouped", weight_bits=8, act_q8_0=1), T, seed=6)
+
+
+def test_layer_small_softmax_fp32():
+    check_layer(small("softmax", x_dtype="f32"), 21, seed=7)
+
+
+def test_layer_deterministic_and_T0_noop():
+    s = small("grouped")
+    L = get_layer(s, 1)
+    _, xd, *_ = inputs(s, L, 3, 29)
+    a = [t.clone() for t in L.forward(xd)]
+    b = L.forward(xd)
+    for p, q in zip(a, b):
+        assert torch.equal(p, q)
+    empty = torch.empty((0, s.hidden), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((0, s.hidden), dtype=torch.float32, device="cuda")
+    ids = torch.empty((0, s.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((0, s.top_k), dtype=torch.float32, device="cuda")
+    moe.moe_layer_forward(L.cfg, L.packed, empty, out, ids, w, L.ws(1))
+
+
+# full-size layers (the benchmark's shapes); large T checks sampled tokens
+@pytest.mark.parametrize("name,T,sample", [("mixtral", 1, None), ("dsv3", 1, None),
+                                           ("dsv3", 16, 3), ("dsv3", 2048, 2),
+                                           ("dsv3_int2", 1, None), ("dsv3_int8", 4, 2),
+                                           ("dsv3_int8", 64, 2), ("mixtral", 512, 2)])
+def test_layer_full_size(name, T, sample):
+    check_layer(gen.spec(name), T, sample=sample)
+
+
+# ------------------------------------------------------------------ integer paths
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_q8_0_codes_bit_exact(dtype):
+    s = gen.spec("dsv3", x_dtype=dtype)
+    x, bits = gen.hidden_states(s, 9, 0, 12)
+    xd = gen.device.hidden_to_device(s, x, bits)
+    q = torch.empty((12, s.hidden), dtype=torch.int8, device="cuda")
+    d = torch.empty((12, s.hidden // 32), dtype=torch.float32, device="cuda")
+    moe.moe_q8_0_quantize(xd, q, d)
+    torch.cuda.synchronize()
+    qo, do = oracle.q8_0_encode(x.astype(np.float32))
+    assert np.array_equal(q.cpu().numpy().ravel(), qo)
+    assert np.array_equal(d.cpu().numpy().ravel().view(np.uint32), do.view(np.uint32))
+
+
+def test_block_dots_bit_exact():
+    s = gen.spec("dsv3_int8")
+    L = get_layer(s)
+    x, bits = gen.hidden_states(s, 10, 0, 3)
+    qx, dx = oracle.q8_0_encode(x.astype(np.float32))
+    qx = qx.reshape(3, s.hidden)
+    rng = np.random.default_rng(0)
+    for e, which in [(3, 0), (3, 1), (200, 2), (256, 0)]:
+        name = ("gate", "up", "down")[which]
+        codes = gen.expert_codes(s, 0, 0, e, name)
+        K = codes.shape[1]
+        rows = rng.choice(codes.shape[0], 5, replace=False).astype(np.int32)
+        qa = qx if which < 2 else rng.integers(-127, 128, (3, K)).astype(np.int8)
+        dots = torch.empty((5, 3, K // 32), dtype=torch.int32, device="cuda")
+        moe.moe_debug_block_dots(L.cfg, L.packed, e, which, torch.from_numpy(rows).cuda(),
+                                 torch.from_numpy(np.ascontiguousarray(qa)).cuda(), dots)
+        torch.cuda.synchronize()
+        got = dots.cpu().numpy()
+        for ri, r in enumerate(rows):
+            for t in range(3):
+                for b in range(K // 32):
+                    ref = oracle.block_dot(codes[r, b * 32:(b + 1) * 32], qa[t, b * 32:(b + 1) * 32])
+                    assert got[ri, t, b] == ref
+
+
+# ------------------------------------------------------------------ device status
+
+def test_packed_header_mismatch_is_reported():
+    s = small("grouped")
+    L = get_layer(s, 1)
+    _, xd, *_ = inputs(s, L, 4, 4)
+    bad = gen.device.config_for(s)
+    bad.weight_bits = 8  # different layout than the blob holds
+    ws = torch.zeros(moe.moe_workspace_bytes(bad, 4), dtype=torch.uint8, device="cuda")
+    ids = torch.empty((4, s.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((4, s.top_k), dtype=torch.float32, device="cuda")
+    big = torch.zeros(moe.moe_packed_bytes(bad), dtype=torch.uint8, device="cuda")
+    big[: L.packed.numel()].copy_(L.packed)
+    moe.moe_route_topk(bad, big, xd, ids, w, ws)
+    assert moe.moe_read_status(ws) == moe.MOE_ERR_PACKED
+    assert moe.moe_read_status(ws) == moe.MOE_OK  # read clears
+
+
+def test_bounded_wait_gives_up_with_timeout_status():
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    moe.moe_debug_wait_timeout(ws, 1000)
+    assert moe.moe_read_status(ws) == moe.MOE_ERR_TIMEOUT
+    # the context is still usable afterwards
+    t = torch.ones(16, device="cuda")
+    assert float(t.sum()) == 16.0
