@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of one DeepSeek-V3-style MoE layer forward on GB300.
+
+Workload (seeded, synthetic): H=6144, I=2048, 256 routed experts + 1 shared, sigmoid
+grouped router (8 groups, 4 kept, top-8, routed_scaling_factor 2.5), int4 per-row-scaled
+weights, bf16 hidden states N(0,1).  One step = one layer forward at each of T = 1
+(decode), 16 (a verify batch) and 2048 (prefill): 2065 tokens.  Every forward reads its
+own one of 4 rotating input batches, and L2 is flushed (a 512 MB write) before each
+forward, outside the timed events.
+
+`value` is tokens/s over the device-timed forwards (CUDA events on the launching
+stream); `e2e` is the same through pinned host buffers with the copies timed.  Per-T
+results, the per-stage split and the roofline of the dominant kernel are in the line.
+
+--impl reference times the CPU oracle (plain single-threaded fp64 C) on a bounded sample
+of the same workload.
+
+Multi-GPU: the layer forward does not shard across GPUs here; --gpus N (under torchrun)
+runs N independent replicas, one per GPU, and reports their aggregate ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MoE-layer tokens/s at T=1/16/2048; % HBM roofline (decode), % bf16 peak (prefill)")
+TS = (1, 16, 2048)
+N_BATCHES = 4
+FLUSH_BYTES = 512 << 20
+NOMINAL_HBM_GBS = 8000.0  # the "about 8 TB/s" figure the target is quoted against
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    sm_max=d.get("sm_max_mhz", 2070.0), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max=2070.0, src="fallback")
+
+
+def args_():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--T", default=",".join(map(str, TS)),
+                    help="token counts of one step (default: the headline 1,16,2048)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_init(n):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ work accounting
+
+def expert_bytes(s, inter):
+    """packed weight bytes + fp32 row scales of one expert"""
+    return (3 * s.hidden * inter * s.weight_bits) // 8 + (2 * inter + s.hidden) * 4
+
+
+def gate_up_bytes(s, inter):
+    return (2 * s.hidden * inter * s.weight_bits) // 8 + 2 * inter * 4
+
+
+def layer_flops(s, T):
+    return 2 * 3 * s.hidden * (s.inter * T * s.top_k + s.inter_sh * T * s.n_shared)
+
+
+def traffic_record(kernel):
+    """ncu DRAM bytes per launch recorded under profiles/, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != d["sha256"]:
+        return None
+    return d
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(a, rank, ws_n, local):
+    global TS
+    TS = tuple(int(t) for t in a.T.split(","))
+    import numpy as np
+    import torch
+
+    import gen
+    import routed_expert_ffn_route_gb300 as moe
+    from gen.device import build_packed_layer, hidden_to_device
+
+    moe.lib()  # fail loudly if the CUDA library is missing
+    s = gen.spec("dsv3")
+    seed = 0
+    cfg, packed = build_packed_layer(s, seed, 0, "cuda")
+    H, k = s.hidden, s.top_k
+    Tmax = max(TS)
+    ws = torch.zeros(moe.moe_workspace_bytes(cfg, Tmax), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    xs, xh = {}, {}
+    for T in TS:
+        xs[T], xh[T] = [], []
+        for b in range(N_BATCHES):
+            x, bits = gen.hidden_states(s, seed + 1000 * rank, 10 + b, T)
+            xd = hidden_to_device(s, x, bits)
+            xs[T].append(xd)
+            xh[T].append(xd.cpu().pin_memory())
+    out = {T: torch.empty((T, H), dtype=torch.float32, device="cuda") for T in TS}
+    ids = {T: torch.empty((T, k), dtype=torch.int32, device="cuda") for T in TS}
+    w = {T: torch.empty((T, k), dtype=torch.float32, device="cuda") for T in TS}
+    out_h = {T: torch.empty((T, H), dtype=torch.float32).pin_memory() for T in TS}
+    ids_h = {T: torch.empty((T, k), dtype=torch.int32).pin_memory() for T in TS}
+    w_h = {T: torch.empty((T, k), dtype=torch.float32).pin_memory() for T in TS}
+    stream = torch.cuda.current_stream()
+
+    # unique experts per (T, batch), from one untimed pass
+    uniq = {}
+    for T in TS:
+        for b in range(N_BATCHES):
+            moe.moe_layer_forward(cfg, packed, xs[T][b], out[T], ids[T], w[T], ws)
+            uniq[(T, b)] = int(np.unique(ids[T].cpu().numpy()).size)
+    st = moe.moe_read_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.moe_status_str(st)}")
+
+    def step(i, evs):
+        for T in TS:
+            flush.zero_()
+            moe.moe_layer_forward_timed(cfg, packed, xs[T][i % N_BATCHES], out[T], ids[T], w[T],
+                                        ws, evs[T])
+
+    mk = lambda: {T: [torch.cuda.Event(enable_timing=True) for _ in range(7)] for T in TS}
+    for i in range(a.warmup):
+        step(i, mk())
+    torch.cuda.synchronize()
+    events = [mk() for _ in range(a.steps)]
+    clocks = Clocks(local)
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(a.steps):
+        step(a.warmup + i, events[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    barrier(ws_n)
+    st = moe.moe_read_status(ws)
+    if st != moe.MOE_OK:
+        raise RuntimeError(f"device status {moe.moe_status_str(st)}")
+
+    # per (T, stage) device times
+    stage_ms = {T: [0.0] * 6 for T in TS}
+    fwd_ms = {T: 0.0 for T in TS}
+    for ev in events:
+        for T in TS:
+            fwd_ms[T] += ev[T][0].elapsed_time(ev[T][6])
+            for j in range(6):
+                stage_ms[T][j] += ev[T][j].elapsed_time(ev[T][j + 1])
+    total_ms = sum(fwd_ms.values())
+    total_ms_max = allmax(total_ms, ws_n)
+    tokens = a.steps * sum(TS) * ws_n
+    value = tokens / (total_ms_max / 1e3)
+
+    # e2e: pinned host buffers, copies inside the timed region
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(a.steps * len(TS))]
+    barrier(ws_n)
+    torch.cuda.synchronize()
+    n = 0
+    for i in range(a.steps):
+        for T in TS:
+            flush.zero_()
+            e0, e1 = e2e_ev[n]
+            n += 1
+            e0.record()
+            xd = xs[T][i % N_BATCHES]
+            xd.copy_(xh[T][i % N_BATCHES], non_blocking=True)
+            moe.moe_layer_forward(cfg, packed, xd, out[T], ids[T], w[T], ws)
+            out_h[T].copy_(out[T], non_blocking=True)
+            ids_h[T].copy_(ids[T], non_blocking=True)
+            w_h[T].copy_(w[T], non_blocking=True)
+            e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = allmax(sum(e0.elapsed_time(e1) for e0, e1 in e2e_ev), ws_n)
+    h2d = sum(T * H * 2 for T in TS)
+    d2h = sum(T * H * 4 + T * k * 8 for T in TS)
+
+    pk = peaks()
+    by_T = {}
+    for T in TS:
+        ms = fwd_ms[T] / a.steps
+        u = statistics.mean(uniq[(T, b % N_BATCHES)] for b in range(a.warmup, a.warmup + a.steps))
+        ent = {"tokens_per_s": T / (ms / 1e3), "ms": round(ms, 4), "unique_experts": u,
+               "stage_ms": {moe.STAGES[j]: round(stage_ms[T][j] / a.steps, 4) for j in range(6)}}
+        byts = (u + s.n_shared) * expert_bytes(s, s.inter)
+        gbs = byts / (ms / 1e3) / 1e9
+        fl = layer_flops(s, T)
+        tfs = fl / (ms / 1e3) / 1e12
+        ent["hbm"] = {"expert_bytes": byts, "GB/s": round(gbs, 1),
+                      "frac_of_measured": round(gbs / pk["hbm"], 4),
+                      "frac_of_8TBs": round(gbs / NOMINAL_HBM_GBS, 4)}
+        ent["bf16"] = {"flops": fl, "TFLOP/s": round(tfs, 2),
+                       "frac_of_measured_burst": round(tfs / pk["bf16"], 4),
+                       "frac_of_measured_sustained": round(tfs / pk["bf16_sus"], 4)}
+        by_T[str(T)] = ent
+
+    # dominant kernel: the (T, stage) with the largest share of the step
+    dT, dj = max(((T, j) for T in TS for j in range(6)), key=lambda p: stage_ms[p[0]][p[1]])
+    kname = moe.STAGES[dj]
+    avg_ms = stage_ms[dT][dj] / a.steps
+    u = by_T[str(dT)]["unique_experts"]
+    roof = {"kernel": f"{kname} (T={dT})", "share_of_step": round(stage_ms[dT][dj] / total_ms, 4)}
+    if kname == "gate_up":
+        fl = 2 * 2 * s.hidden * (s.inter * dT * k + s.inter_sh * dT * s.n_shared)
+        byts = (u + s.n_shared) * gate_up_bytes(s, s.inter)
+    elif kname == "down":
+        fl = 2 * s.hidden * (s.inter * dT * k + s.inter_sh * dT * s.n_shared)
+        byts = (u + s.n_shared) * (s.hidden * s.inter * s.weight_bits // 8 + s.hidden * 4)
+    else:
+        fl, byts = 0, 0
+    # the expert kernels run on the CUDA cores (fp32 FMA): an ALU bound at large T,
+    # HBM at decode; FFMA peak = SMs x 128 lanes x 2 flop x max SM clock
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    ffma_peak = sms * 128 * 2 * pk["sm_max"] * 1e6 / 1e12
+    if dT >= 256 and fl:
+        ach = fl / (avg_ms / 1e3) / 1e12
+        roof.update({"bound": "alu", "achieved": round(ach, 2), "peak": round(ffma_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(ach / ffma_peak, 4),
+                     "peak_source": f"fp32 FMA: {sms} SMs x 128 lanes x 2 x {pk['sm_max']:.0f} MHz"})
+    else:
+        ach = byts / (avg_ms / 1e3) / 1e9 if byts else 0.0
+        roof.update({"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(ach / pk["hbm"], 4), "peak_source": pk["src"]})
+    tr = traffic_record(f"{kname}_T{dT}")
+    roof["traffic"] = tr["bytes_per_launch"] if tr else None
+    roof["algorithmic_per_launch"] = {"bytes": byts, "flops": fl}
+
+    launches = a.steps * sum(moe.moe_forward_launches(cfg, T) for T in TS)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws_n,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(total_ms_max / a.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "DeepSeek-V3-style MoE layer: H=6144 I=2048 E=256+1 shared top-8, "
+                               "sigmoid grouped router (8 groups, keep 4), int4 per-row-scaled "
+                               "weights, bf16 x; one step = forwards at T=1, 16, 2048",
+                   "tokens_per_step": sum(TS), "T": list(TS), "input_batches": N_BATCHES,
+                   "l2": "flushed (512 MB write) before every forward, outside the timed events",
+                   "parallelism": f"replicas x{ws_n}"},
+        "by_T": by_T,
+        "roofline": roof,
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if rank == 0 and ws_n == 1 and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(s, seed, ntok=2)
+    return line
+
+
+# ------------------------------------------------------------------ the oracle (CPU baseline)
+
+def _oracle_token_fixture(s, seed, batch, t):
+    """host inputs for one token: x row, the oracle router weights, its selected experts"""
+    import numpy as np
+
+    import gen
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from _support import make_experts, shared_expert
+    x, _ = gen.hidden_states(s, seed, batch, t + 1, rows=[t])
+    wr, bias = gen.router_weights(s, seed), gen.router_bias(s, seed)
+    ids, _, _ = oracle.route(s, oracle.router_logits(s, x.astype(np.float64), wr), bias)
+    experts = make_experts(s, seed, 0, sorted(set(int(e) for e in ids.ravel())))
+    return x.astype(np.float64), wr, bias, experts, shared_expert(s, seed, 0)
+
+
+def cpu_baseline(s, seed, ntok):
+    import oracle
+    oracle.build()
+    fx = [_oracle_token_fixture(s, seed, 10, t) for t in range(ntok)]
+    t0 = time.perf_counter()
+    for x, wr, bias, experts, sh in fx:
+        oracle.layer_forward(s, x, wr, bias, experts, sh, mode=1)
+    dt = time.perf_counter() - t0
+    return {"value": round(ntok / dt, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{ntok} tokens of the same DSV3-style layer through the fp64 oracle "
+                      "(router over all 256 experts + 8 routed + shared SwiGLU experts, "
+                      "single thread); per-token work is independent of T",
+            "seconds": round(dt, 2), "host_cpus": os.cpu_count()}
+
+
+def run_reference(a, rank, ws_n):
+    import gen
+    import oracle
+    if rank != 0:
+        return None
+    oracle.build()
+    s = gen.spec("dsv3")
+    pool = [_oracle_token_fixture(s, 0, 10, t) for t in range(4)]
+    for i in range(a.warmup):
+        x, wr, bias, ex, sh = pool[i % 4]
+        oracle.layer_forward(s, x, wr, bias, ex, sh, mode=1)
+    t0 = time.perf_counter()
+    for i in range(a.steps):
+        x, wr, bias, ex, sh = pool[(a.warmup + i) % 4]
+        oracle.layer_forward(s, x, wr, bias, ex, sh, mode=1)
+    dt = time.perf_counter() - t0
+    v = round(a.steps / dt, 4)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws_n,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(dt / a.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "DeepSeek-V3-style MoE layer (same as our arm); each reference "
+                               "step = one token through the fp64 CPU oracle",
+                   "parallelism": "single CPU thread"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{a.steps} tokens, one per step, from a pool of 4 seeded "
+                                   "tokens of the DSV3-style layer"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    a = args_()
+    rank, ws_n, local = dist_init(a.gpus)
+    if a.impl == "reference":
+        line = run_reference(a, rank, ws_n)
+    else:
+        line = run_ours(a, rank, ws_n, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws_n > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -149,6 +149,19 @@ int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const voi
                       moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
                       size_t ws_bytes, void *stream);
 
+/* moe_layer_forward with stage timing: records the caller's CUDA events (cudaEvent_t
+ * passed as void*) on `stream` around the stages, events[0] before the first kernel and
+ * events[i+1] after stage i, for the stages 0 router (logits + top-k), 1 permutation,
+ * 2 Q8_0 activation encoding (empty unless act_q8_0), 3 gate/up + SwiGLU, 4 down
+ * projection, 5 combine.  n_events must be >= 7.  Same results as moe_layer_forward. */
+int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, const void *x,
+                            moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
+                            size_t ws_bytes, void *const *events, int n_events, void *stream);
+
+/* Number of kernel launches one moe_layer_forward makes for `cfg` and T tokens
+ * (0 for T == 0; negative moe_status for an unsupported config). */
+int moe_forward_launches(const moe_layer_config *cfg, int T);
+
 /* Synchronise `stream`, then return and clear the device status word of `ws`
  * (MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_NUMERIC, MOE_ERR_PACKED). */
 int moe_read_status(void *ws, void *stream);

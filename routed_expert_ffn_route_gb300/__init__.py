@@ -37,8 +37,11 @@ EXPORTED = [
     "moe_workspace_bytes", "moe_pack_weights", "moe_pack_router", "moe_pack_expert",
     "moe_unpack_weights", "moe_route_topk", "moe_layer_forward", "moe_read_status",
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
-    "moe_debug_wait_timeout",
+    "moe_debug_wait_timeout", "moe_layer_forward_timed", "moe_forward_launches",
 ]
+
+# stages bracketed by the events of moe_layer_forward_timed
+STAGES = ["router", "permute", "q8_encode", "gate_up", "down", "combine"]
 
 
 class MoEError(RuntimeError):
@@ -103,6 +106,8 @@ def _bind(L):
         "moe_q8_0_quantize": (I, [P, I, I, I, P, P, P]),
         "moe_debug_block_dots": (I, [P, P, I, I, P, I, P, I, P, P]),
         "moe_debug_wait_timeout": (I, [P, S, I, P]),
+        "moe_layer_forward_timed": (I, [P, P, P, I, I, P, P, P, P, S, P, I, P]),
+        "moe_forward_launches": (I, [P, I]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -207,6 +212,22 @@ def moe_layer_forward(cfg, packed, x, out, ids, w, ws, stream=None):
     T = x.shape[0]
     _ck(lib().moe_layer_forward(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out), _p(ids),
                                 _p(w), _p(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_timed(cfg, packed, x, out, ids, w, ws, events, stream=None):
+    """events: 7 torch.cuda.Event(enable_timing=True); see STAGES for what they bracket."""
+    T = x.shape[0]
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event lazily, on its first record
+            e.record()
+    arr = (C.c_void_p * len(events))(*[C.c_void_p(e.cuda_event) for e in events])
+    _ck(lib().moe_layer_forward_timed(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out),
+                                      _p(ids), _p(w), _p(ws), ws.numel(), arr, len(events),
+                                      _stream(stream)), "moe_layer_forward_timed")
+
+
+def moe_forward_launches(cfg, T) -> int:
+    return lib().moe_forward_launches(C.byref(cfg), int(T))
 
 
 def moe_read_status(ws, stream=None) -> int:

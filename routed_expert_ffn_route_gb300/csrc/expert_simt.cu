@@ -325,7 +325,7 @@ static int launch_persistent(K kern, size_t smem, int item_bound, const ExpertAr
 }
 
 template <int BITS, int GN, bool Q8>
-static int run_experts(const moe_layer_config &c, const ExpertArgs &a, const WsLayout &W,
+static int run_experts(const moe_layer_config &c, const ExpertArgs &a, const WsLayout &W, void *mid,
                        cudaStream_t st) {
   const int mt_s = a.LS.inter / 64, mt_r = a.LR.inter / 64, mt_n = a.H / kTileRows;
   const int max_routed = W.max_groups - a.ns;
@@ -336,28 +336,30 @@ static int run_experts(const moe_layer_config &c, const ExpertArgs &a, const WsL
                       : (size_t)GN * a.Imax * 4;
   int r = launch_persistent(gate_up_kernel<BITS, GN, Q8>, smem_gu, bound_gu, a, st);
   if (r) return r;
+  if (mid && cudaEventRecord((cudaEvent_t)mid, st) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_persistent(down_kernel<BITS, GN, Q8>, smem_dn, bound_dn, a, st);
 }
 
 template <int BITS, bool Q8>
-static int run_gn(const moe_layer_config &c, const ExpertArgs &a, const WsLayout &W,
+static int run_gn(const moe_layer_config &c, const ExpertArgs &a, const WsLayout &W, void *mid,
                   cudaStream_t st) {
   switch (W.group_n) {
-    case 1: return run_experts<BITS, 1, Q8>(c, a, W, st);
-    case 2: return run_experts<BITS, 2, Q8>(c, a, W, st);
-    case 4: return run_experts<BITS, 4, Q8>(c, a, W, st);
-    default: return run_experts<BITS, 8, Q8>(c, a, W, st);
+    case 1: return run_experts<BITS, 1, Q8>(c, a, W, mid, st);
+    case 2: return run_experts<BITS, 2, Q8>(c, a, W, mid, st);
+    case 4: return run_experts<BITS, 4, Q8>(c, a, W, mid, st);
+    default: return run_experts<BITS, 8, Q8>(c, a, W, mid, st);
   }
 }
 
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
-                   moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st) {
+                   moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
+                   void *mid) {
   ExpertArgs a = make_args(c, packed, x, dt, T, ws, W);
-  if (c.act_q8_0) return run_gn<8, true>(c, a, W, st);
+  if (c.act_q8_0) return run_gn<8, true>(c, a, W, mid, st);
   switch (c.weight_bits) {
-    case 4: return run_gn<4, false>(c, a, W, st);
-    case 2: return run_gn<2, false>(c, a, W, st);
-    default: return run_gn<8, false>(c, a, W, st);
+    case 4: return run_gn<4, false>(c, a, W, mid, st);
+    case 2: return run_gn<2, false>(c, a, W, mid, st);
+    default: return run_gn<8, false>(c, a, W, mid, st);
   }
 }
 

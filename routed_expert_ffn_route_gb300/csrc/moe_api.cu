@@ -210,9 +210,9 @@ int moe_route_topk(const moe_layer_config *cfg, const void *packed, const void *
   return launch_router(*cfg, (const uint8_t *)packed, x, dtype, T, ids, w, (uint8_t *)ws, W, st);
 }
 
-int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const void *x,
-                      moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
-                      size_t ws_bytes, void *stream) {
+static int forward_impl(const moe_layer_config *cfg, const void *packed, const void *x,
+                        moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
+                        size_t ws_bytes, void *const *ev, void *stream) {
   WsLayout W;
   int r = common_args(cfg, packed, x, dtype, T, ids, w, ws, ws_bytes, &W);
   if (r || T == 0) return r;
@@ -220,12 +220,43 @@ int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const voi
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t *wsb = (uint8_t *)ws;
   const uint8_t *pk = (const uint8_t *)packed;
-  if (cudaMemsetAsync(ws, 0, sizeof(Ctrl), st) != cudaSuccess) return MOE_ERR_CUDA;
+  auto mark = [&](int i) {
+    return ev ? cudaEventRecord((cudaEvent_t)ev[i], st) == cudaSuccess : true;
+  };
+  if (cudaMemsetAsync(ws, 0, sizeof(Ctrl), st) != cudaSuccess || !mark(0)) return MOE_ERR_CUDA;
   if ((r = launch_router(*cfg, pk, x, dtype, T, ids, w, wsb, W, st))) return r;
+  if (!mark(1)) return MOE_ERR_CUDA;
   if ((r = launch_permute(*cfg, T, ids, wsb, W, st))) return r;
+  if (!mark(2)) return MOE_ERR_CUDA;
   if (cfg->act_q8_0 && (r = launch_quant_x(*cfg, x, dtype, T, wsb, W, st))) return r;
-  if ((r = launch_experts(*cfg, pk, x, dtype, T, wsb, W, st))) return r;
-  return launch_combine(*cfg, T, w, out, wsb, W, st);
+  if (!mark(3)) return MOE_ERR_CUDA;
+  if ((r = launch_experts(*cfg, pk, x, dtype, T, wsb, W, st, ev ? ev[4] : nullptr))) return r;
+  if (!mark(5)) return MOE_ERR_CUDA;
+  if ((r = launch_combine(*cfg, T, w, out, wsb, W, st))) return r;
+  return mark(6) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const void *x,
+                      moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
+                      size_t ws_bytes, void *stream) {
+  return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, const void *x,
+                            moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
+                            size_t ws_bytes, void *const *events, int n_events, void *stream) {
+  if (!events || n_events < 7) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 7; i++)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, events, stream);
+}
+
+int moe_forward_launches(const moe_layer_config *cfg, int T) {
+  int r = check(cfg);
+  if (r) return r;
+  if (T <= 0) return 0;
+  // router logits + top-k, permute, [Q8_0 encode], gate/up, down, combine
+  return 2 + 1 + (cfg->act_q8_0 ? 1 : 0) + 2 + 1;
 }
 
 int moe_read_status(void *ws, void *stream) {

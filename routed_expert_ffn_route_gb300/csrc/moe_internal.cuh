@@ -153,8 +153,10 @@ int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t
                    const WsLayout &W, cudaStream_t st);
 int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
+// mid_event (a cudaEvent_t or null) is recorded between the gate/up and down launches
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
-                   moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st);
+                   moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
+                   void *mid_event);
 int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
 int launch_pack_expert(const moe_layer_config &c, const ExpertLayout &L, const int8_t *gate,
