@@ -158,6 +158,27 @@ int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, con
                             moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
                             size_t ws_bytes, void *const *events, int n_events, void *stream);
 
+/* Allocation-free moe_layer_forward, for callers that cannot provide device scratch
+ * (plugin hosts that pass an op only its input and output tensors, serving loops whose
+ * device memory is fixed at start-up, code that must not call cudaMalloc because it may
+ * synchronise the device).  The pages have no counterpart: it is a property of this
+ * library's interface, not of the method.
+ * Same kernels and results as moe_layer_forward; the scratch is a file-scope device array
+ * of 8 MiB inside the library, held by every GPU that loads the library until the
+ * process exits.  Calls whose workspace (moe_workspace_bytes(cfg, T)) exceeds 8 MiB are
+ * rejected with MOE_ERR_WORKSPACE (for the DeepSeek-V3-style layer: T <= 16).  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  No cudaMalloc,
+ * cudaFree or allocating routine is called.  All calls on a device share the one array,
+ * which keeps the last call's contents (each call clears the status word it uses first):
+ * calls that overlap on the GPU (issued on different streams, or from several host
+ * threads without ordering) race on it, so serialise them.  status: optional device int32 that receives the
+ * device status word (MOE_OK, MOE_ERR_NUMERIC, MOE_ERR_PACKED ...) at the end of the call,
+ * stream-ordered; may be NULL. */
+int moe_layer_forward_static(const moe_layer_config *cfg, const void *packed, const void *x,
+                             moe_dtype dtype, int T, float *out, int32_t *ids, float *w,
+                             int32_t *status, void *stream);
+
 /* Number of kernel launches one moe_layer_forward makes for `cfg` and T tokens
  * (0 for T == 0; negative moe_status for an unsupported config). */
 int moe_forward_launches(const moe_layer_config *cfg, int T);

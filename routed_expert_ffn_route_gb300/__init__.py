@@ -38,6 +38,7 @@ EXPORTED = [
     "moe_unpack_weights", "moe_route_topk", "moe_layer_forward", "moe_read_status",
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
     "moe_debug_wait_timeout", "moe_layer_forward_timed", "moe_forward_launches",
+    "moe_layer_forward_static",
 ]
 
 # stages bracketed by the events of moe_layer_forward_timed
@@ -108,6 +109,7 @@ def _bind(L):
         "moe_debug_wait_timeout": (I, [P, S, I, P]),
         "moe_layer_forward_timed": (I, [P, P, P, I, I, P, P, P, P, S, P, I, P]),
         "moe_forward_launches": (I, [P, I]),
+        "moe_layer_forward_static": (I, [P, P, P, I, I, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -224,6 +226,14 @@ def moe_layer_forward_timed(cfg, packed, x, out, ids, w, ws, events, stream=None
     _ck(lib().moe_layer_forward_timed(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out),
                                       _p(ids), _p(w), _p(ws), ws.numel(), arr, len(events),
                                       _stream(stream)), "moe_layer_forward_timed")
+
+
+def moe_layer_forward_static(cfg, packed, x, out, ids, w, status=None, stream=None):
+    """Allocation-free forward: scratch lives in the library's own 8 MiB device array."""
+    T = x.shape[0]
+    _ck(lib().moe_layer_forward_static(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out),
+                                       _p(ids), _p(w), _p(status), _stream(stream)),
+        "moe_layer_forward_static")
 
 
 def moe_forward_launches(cfg, T) -> int:
