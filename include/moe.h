@@ -164,8 +164,8 @@ int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, con
  * synchronise the device).  The pages have no counterpart: it is a property of this
  * library's interface, not of the method.
  * Same kernels and results as moe_layer_forward; the scratch is a file-scope device array
- * of 8 MiB inside the library, held by every GPU that loads the library until the
- * process exits.  Calls whose workspace (moe_workspace_bytes(cfg, T)) exceeds 8 MiB are
+ * of 32 MiB inside the library, held by every GPU that loads the library until the
+ * process exits.  Calls whose workspace (moe_workspace_bytes(cfg, T)) exceeds 32 MiB are
  * rejected with MOE_ERR_WORKSPACE (for the DeepSeek-V3-style layer: T <= 16).  The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  No cudaMalloc,

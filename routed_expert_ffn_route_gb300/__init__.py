@@ -229,7 +229,7 @@ def moe_layer_forward_timed(cfg, packed, x, out, ids, w, ws, events, stream=None
 
 
 def moe_layer_forward_static(cfg, packed, x, out, ids, w, status=None, stream=None):
-    """Allocation-free forward: scratch lives in the library's own 8 MiB device array."""
+    """Allocation-free forward: scratch lives in the library's own 32 MiB device array."""
     T = x.shape[0]
     _ck(lib().moe_layer_forward_static(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out),
                                        _p(ids), _p(w), _p(status), _stream(stream)),

@@ -354,6 +354,7 @@ static int run_gn(const moe_layer_config &c, const ExpertArgs &a, const WsLayout
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
                    void *mid) {
+  if (W.tc) return launch_experts_tc(c, packed, x, dt, T, ws, W, st, mid);
   ExpertArgs a = make_args(c, packed, x, dt, T, ws, W);
   if (c.act_q8_0) return run_gn<8, true>(c, a, W, mid, st);
   switch (c.weight_bits) {

@@ -1,0 +1,532 @@
+// expert_tc.cu -- the grouped SwiGLU expert GEMMs on the 5th-generation tensor cores.
+//
+// Expert FFN ("企业官网建设流程全解析", §3.1 激活内存池化: SwiGLU gate_proj; "Show HN: 如何在我的
+// 低配置电脑上运行 GLM-5.2", 已实现的功能: routed-expert SwiGLU, 量化内核 int8/int4/int2 逐行缩放,
+// 使用时反量化; "colibrì 深度拆解", §5.1 per-row scaled int4):
+//   g = s_g * (Q_g x),  u = s_u * (Q_u x),  h = silu(g) * u,  y = s_d * (Q_d h)
+//
+// Tensor-core formulation (one CTA per SM, persistent over (group, m-tile) work items):
+//   D[128 weight rows][N] (fp32, TMEM) += A[128][K] * B[N][K]^T
+//   A = codes of 128 weight rows, dequantised to exact small integers in bf16 (gate/up,
+//       against bf16 x) or fp16 (down, against fp16 h) and written to TMEM, so the weight
+//       operand costs no shared-memory read bandwidth (tcgen05.mma with A in TMEM);
+//   B = the group's activation rows (<= 128 tokens x pieces, padded to a multiple of 8), a
+//       128-byte-swizzled K-major tile produced in that exact layout in global memory; the
+//       MMA's N is the row count rounded up to 16, and the extra rows it reads only feed
+//       accumulator columns the epilogue never reads;
+//   the fp32 per-row scale factors out of each dot and is applied in the epilogue.
+//
+// The K dimension streams in 64-element chunks.  Operands move in runs of several chunks
+// per bulk copy (codes: RA chunks = RA x 4 KB at int4; activation tiles: RB chunks), so
+// the hand-off latency of a copy (its stage must first be released by the consumers) is
+// paid once per run.  A chunk's dequantised codes live in one of up to 15 TMEM stages
+// (32 columns each) next to the accumulators.
+//
+// Warp roles: 20 code producer and 21 activation-tile producer (bulk copies, one thread
+// each), 0-3 MMA issuers (one thread each, taking turns by chunk, each into its own TMEM
+// accumulator), 8-19 dequantisers in three sets that take turns by chunk (one weight row
+// per thread, smem -> registers -> TMEM), 4-7 epilogue (TMEM -> registers, sum of the
+// issuers' accumulators, scale, SwiGLU, stores).  Every wait is bounded: a wait that gives up
+// records MOE_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained and TMEM
+// is freed before exit.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "dev.cuh"
+#include "expert_args.cuh"
+#include "moe_internal.cuh"
+#include "tc.cuh"
+
+namespace moe {
+
+// Pipeline tracing for development builds (-DMOE_TRACE): the SM clock at each hand-off of
+// the first kTraceChunks chunks of CTA 0, one row of kTraceChunks per event.
+constexpr int kTraceChunks = 256;
+#ifdef MOE_TRACE
+#define MOE_TC_TRACE(ev, c)                                               \
+  do {                                                                    \
+    if (blockIdx.x == 0 && a.trace && (c) < kTraceChunks)                 \
+      a.trace[(ev) * kTraceChunks + (c)] = (long long)clock64();          \
+  } while (0)
+static long long *g_trace = nullptr;
+extern "C" void moe_trace_set(void *buf) { g_trace = (long long *)buf; }
+#else
+#define MOE_TC_TRACE(ev, c) \
+  do {                      \
+  } while (0)
+#endif
+
+// warps: 0-3 MMA issuers (0 also owns TMEM), 4-7 epilogue, 8-19 dequantiser sets (4 warps
+// each: one per TMEM lane quarter), 20 code producer, 21 activation-tile producer
+constexpr int kDqSets = 3;
+constexpr int kDqWarp0 = 8;
+constexpr int kProdWarp0 = kDqWarp0 + 4 * kDqSets;
+constexpr int kWarps = kProdWarp0 + 2;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxIssuers = 4;
+constexpr int kMaxStages = 16;
+constexpr int kMaxRuns = 24;
+
+// MMA issuer threads take turns by chunk, each accumulating into its own TMEM accumulator
+// (NMAX columns, NMAX = the launch's largest B row count); the epilogue sums them.  A
+// thread waits ~100-150 cycles per tcgen05 instruction it issues, so two issuers keep the
+// tensor pipe fed (every item has at least two chunks, so both always contribute).  TMEM
+// (512 columns) holds the accumulators and up to 15 chunk stages of dequantised codes (32
+// columns each).  Shared memory holds the code-run ring and the activation-tile ring.
+template <int NMAX>
+struct Plan {
+  static constexpr int issuers = 2;
+  static constexpr int stages_fit = (512 - issuers * NMAX) / 32;
+  static constexpr int stages = stages_fit < kMaxStages ? stages_fit : kMaxStages;
+  static constexpr int acc_col = stages * 32;
+  static constexpr int a_ring = NMAX <= 32 ? 96 * 1024 : 64 * 1024;
+  static constexpr int b_ring = NMAX <= 32 ? 112 * 1024 : 128 * 1024;
+};
+
+struct TcBars {
+  uint64_t a_full[kMaxRuns], a_empty[kMaxRuns];  // code runs (smem)
+  uint64_t b_full[kMaxRuns], b_empty[kMaxRuns];  // activation-tile runs (smem)
+  uint64_t t_full[kMaxStages];                   // codes dequantised into a TMEM stage
+  uint64_t done[kMaxStages];                     // the chunk's MMAs completed
+  uint64_t acc_full, acc_empty;
+  uint64_t drain[kMaxIssuers];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int NMAX>
+constexpr size_t tc_smem() {
+  return 1024 + (size_t)Plan<NMAX>::a_ring + Plan<NMAX>::b_ring + sizeof(TcBars);
+}
+
+__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t v, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t v, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(b));
+  return r;
+}
+
+// One weight row's 64 codes (one k-chunk) -> 32 pairs of exact 16-bit integers (element
+// 2c in the low half of column c).  F16: fp16 pairs (down); else bf16 pairs (gate/up).
+// Rows are 32 B apart at int4: lanes read the two 16-byte halves in an order that puts
+// the 8 lanes of each shared-memory phase on distinct banks.
+template <int BITS, bool F16>
+__device__ __forceinline__ void dequant_row(const uint8_t *src, int lane, uint32_t (&o)[32]) {
+  if (BITS == 4) {
+    const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;  // 1024 / 128 in both halves
+    const uint32_t bias = F16 ? 0x64086408u : 0x43084308u;   // 1032 / 136: magic + 8
+    const int h0 = (lane >> 2) & 1;
+    const uint4 ua = ((const uint4 *)src)[h0], ub = ((const uint4 *)src)[h0 ^ 1];
+    const uint4 u0 = h0 ? ub : ua, u1 = h0 ? ua : ub;
+    uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+#pragma unroll
+      for (int p = 0; p < 4; p++) {
+        uint32_t v = ((w[i] >> (4 * p)) & 0x000F000Fu) | magic;
+        o[4 * i + p] = F16 ? sub_f16x2(v, bias) : sub_bf16x2(v, bias);
+      }
+  } else if (BITS == 2) {
+    const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;
+    const uint32_t bias = F16 ? 0x64026402u : 0x43024302u;  // magic + 2
+    uint4 u0 = ((const uint4 *)src)[0];
+    uint32_t w[4] = {u0.x, u0.y, u0.z, u0.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++)
+#pragma unroll
+      for (int p = 0; p < 8; p++) {
+        uint32_t v = ((w[i] >> (2 * p)) & 0x00030003u) | magic;
+        o[8 * i + p] = F16 ? sub_f16x2(v, bias) : sub_bf16x2(v, bias);
+      }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      uint4 u = ((const uint4 *)src)[q];
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        float f0 = (float)(int8_t)(w[i] & 0xFF), f1 = (float)(int8_t)((w[i] >> 8) & 0xFF);
+        float f2 = (float)(int8_t)((w[i] >> 16) & 0xFF), f3 = (float)(int8_t)(w[i] >> 24);
+        if (F16) {
+          __half2 a = __floats2half2_rn(f0, f1), b = __floats2half2_rn(f2, f3);
+          o[8 * q + 2 * i] = *(uint32_t *)&a;
+          o[8 * q + 2 * i + 1] = *(uint32_t *)&b;
+        } else {
+          __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
+          o[8 * q + 2 * i] = *(uint32_t *)&a;
+          o[8 * q + 2 * i + 1] = *(uint32_t *)&b;
+        }
+      }
+    }
+  }
+}
+
+template <int BITS, bool DOWN, int NMAX>
+__global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int item_bound) {
+  using PL = Plan<NMAX>;
+  constexpr int ST = PL::stages, NI = PL::issuers;
+  constexpr int AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
+  extern __shared__ uint8_t smraw[];
+  uint8_t *base = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t *bring = base;
+  uint8_t *aring = base + PL::b_ring;
+  TcBars *bars = (TcBars *)(aring + PL::a_ring);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int where = DOWN ? kKDown : kKGateUp;
+  // ring geometry of this launch
+  const int ra = a.ra, rb = a.rb;
+  const int a_run = ra * AB;                                  // bytes of a code run
+  const int b_stride = (rb + (rb > 1 ? 1 : 0)) * NMAX * 128;  // run + the MMA's over-read
+  const int SA = min(kMaxRuns, PL::a_ring / a_run), SB = min(kMaxRuns, PL::b_ring / b_stride);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SA; s++) {
+      tc::mbar_init(&bars->a_full[s], 1);
+      tc::mbar_init(&bars->a_empty[s], 128 * ra);  // every dequantiser thread of every chunk
+    }
+    for (int s = 0; s < SB; s++) {
+      tc::mbar_init(&bars->b_full[s], 1);
+      tc::mbar_init(&bars->b_empty[s], rb < NI ? rb : NI);  // issuers with a chunk in the run
+    }
+    for (int s = 0; s < ST; s++) {
+      tc::mbar_init(&bars->t_full[s], 128);
+      tc::mbar_init(&bars->done[s], 1);
+    }
+    tc::mbar_init(&bars->acc_full, NI);
+    tc::mbar_init(&bars->acc_empty, 128);
+    for (int i = 0; i < NI; i++) tc::mbar_init(&bars->drain[i], 1);
+    bars->abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc<512>(&bars->tmem_base);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+  volatile int *abort = &bars->abort_flag;
+  const long lim = a.wait_limit;
+  auto give_up = [&]() {
+    if (!*abort) { *abort = 1; record_status(a.ctrl, MOE_ERR_TIMEOUT, where); }
+  };
+
+  if (warp >= kProdWarp0) {
+    // ------------------------------------------------ producers: one bulk copy per run
+    if (lane == 0) {
+      const bool isA = warp == kProdWarp0;
+      const int R = isA ? ra : rb, S = isA ? SA : SB;
+      uint64_t *full = isA ? bars->a_full : bars->b_full;
+      uint64_t *empty = isA ? bars->a_empty : bars->b_empty;
+      uint32_t armed = 0, last_ph = 0;
+      int run = 0;
+      bool ok = true;
+      Item it;
+      for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
+        if (!tc_item<DOWN>(a, item, it)) break;
+        for (int kc = 0; kc < it.KC; kc += R, run++) {
+          const int s = run % S;
+          const uint32_t ph = (run / S) & 1;
+          if (!tc::mbar_wait(&empty[s], ph ^ 1, abort, lim)) { ok = false; break; }
+          if (isA) {
+            tc::mbar_arrive_expect_tx(&full[s], (uint32_t)a_run);
+            tc::bulk_g2s(aring + s * a_run, a_src<BITS, DOWN>(a, it, kc), a_run, &full[s]);
+            MOE_TC_TRACE(0, run * R);
+          } else {
+            const uint32_t bytes = (uint32_t)R * it.rows8 * 128;
+            tc::mbar_arrive_expect_tx(&full[s], bytes);
+            tc::bulk_g2s(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes, &full[s]);
+            MOE_TC_TRACE(1, run * R);
+          }
+          armed |= 1u << s;
+          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+        }
+      }
+      if (!ok) {
+        give_up();
+        // let every copy this thread started land before the CTA exits
+        for (int q = 0; q < S; q++)
+          if ((armed >> q) & 1) wait_nofail(&full[q], (last_ph >> q) & 1, lim);
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------ MMA issuers: chunk c goes to c % NI
+    if (lane == 0 && warp < NI) {
+      const int me = warp;
+      int c = 0, n = 0;
+      bool ok = true, issued = false;
+      Item it;
+      for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
+        if (!tc_item<DOWN>(a, item, it)) break;
+        if (!tc::mbar_wait(&bars->acc_empty, (n & 1) ^ 1, abort, lim)) { ok = false; break; }
+        tc::fence_after_sync();
+        const uint32_t idesc = tc::idesc_f16(DOWN ? 0 : 1, it.Npad);
+        const uint32_t dcol = tbase + PL::acc_col + me * NMAX;
+        bool first = true;
+        for (int kc = 0; kc < it.KC; kc++, c++) {
+          if (c % NI != me) continue;
+          const int st = c % ST, brun = c / rb, sb = brun % SB;
+          const uint32_t pt = (c / ST) & 1, pb = (brun / SB) & 1;
+          if (!tc::mbar_wait(&bars->t_full[st], pt, abort, lim) ||
+              !tc::mbar_wait(&bars->b_full[sb], pb, abort, lim)) { ok = false; break; }
+          tc::fence_after_sync();
+          MOE_TC_TRACE(5, c);
+          const uint32_t bsm = tc::smem_u32(bring + sb * b_stride) + (c % rb) * it.rows8 * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++)
+            tc::mma_ts(dcol, tbase + st * 32 + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
+                       !(first && kk == 0));
+          first = false;
+          issued = true;
+          MOE_TC_TRACE(3, c);
+          tc::mma_commit(&bars->done[st]);
+          if ((c + NI) / rb != brun || kc + NI >= it.KC)  // my last chunk of the run
+            tc::mma_commit(&bars->b_empty[sb]);
+          MOE_TC_TRACE(6, c);
+        }
+        if (!ok) break;
+        tc::mma_commit(&bars->acc_full);
+      }
+      if (!ok) {
+        give_up();
+        if (issued) {  // all MMAs issued so far complete before TMEM is freed
+          tc::mma_commit(&bars->drain[me]);
+          wait_nofail(&bars->drain[me], 0, lim);
+        }
+      }
+    }
+  } else if (warp >= kDqWarp0) {
+    // ------------------------------------------------ dequantisers: one weight row a thread
+    const int q = warp & 3, r = 32 * q + lane, set = (warp - kDqWarp0) >> 2;
+    const uint32_t tlane = (uint32_t)(32 * q) << 16;
+    int c = 0;  // running chunk index over all items of this CTA (all roles count alike)
+    bool ok = true;
+    Item it;
+    for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
+      if (!tc_item<DOWN>(a, item, it)) break;
+      for (int kc = 0; kc < it.KC; kc++, c++) {
+        if (c % kDqSets != set) continue;
+        const int arun = c / ra, sa = arun % SA, st = c % ST;
+        const uint32_t pa = (arun / SA) & 1, pt = (c / ST) & 1;
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->a_full[sa], pa, abort, lim));
+        if (!ok) break;
+        if (r == 0) MOE_TC_TRACE(2, c);
+        uint32_t v[32];
+        dequant_row<BITS, DOWN>(aring + sa * a_run + (c % ra) * AB + r * RB, lane, v);
+        tc::mbar_arrive(&bars->a_empty[sa]);
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[st], pt ^ 1, abort, lim));
+        if (!ok) break;
+        tc::fence_after_sync();
+        tc::tmem_st32(tbase + tlane + st * 32, v);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&bars->t_full[st]);
+        if (r == 0) MOE_TC_TRACE(4, c);
+      }
+    }
+    if (!ok && lane == 0) give_up();
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------ epilogue: one output row a thread
+    const int q = warp & 3, r = 32 * q + lane;
+    const uint32_t tlane = (uint32_t)(32 * q) << 16;
+    const uint32_t d0 = tbase + tlane + PL::acc_col;
+    // sum of the issuers' accumulators, 16 columns from c0
+    auto load_sum = [&](int c0, float (&v)[16]) {
+#pragma unroll
+      for (int i = 0; i < NI; i++) {
+        uint32_t t[16];
+        tc::tmem_ld16(d0 + i * NMAX + c0, t);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int jj = 0; jj < 16; jj++) v[jj] = (i ? v[jj] : 0.f) + __uint_as_float(t[jj]);
+      }
+    };
+    int n = 0;
+    bool ok = true;
+    Item it;
+    for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
+      if (!tc_item<DOWN>(a, item, it)) break;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->acc_full, n & 1, abort, lim));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const ExpertLayout &L = it.sh ? a.LS : a.LR;
+      const int gn = it.g.n;
+      if (!DOWN) {
+        const float s = ((const float *)(it.ebase + L.sgu_off))[it.mt * 128 + r];
+        const int j = r >> 1;  // output index within the m-tile (64 outputs)
+        uint8_t *hbase =
+            a.hg + (size_t)it.g.hrow0 * a.Imax * 2 + (size_t)it.mt * round8(gn) * 128;
+        bool bad = false;
+        for (int c0 = 0; c0 < it.Npad; c0 += 16) {
+          float acc[16];
+          load_sum(c0, acc);
+#pragma unroll
+          for (int jj = 0; jj < 16; jj++) {
+            if (a.P == 2 && (jj & 1)) continue;  // the lo piece, folded into its hi column
+            float v = acc[jj];
+            if (a.P == 2) v += acc[(jj + 1) & 15];
+            v *= s;
+            const float up = __shfl_xor_sync(0xffffffffu, v, 1);
+            const int i = (c0 + jj) / a.P;  // token within the group
+            if ((r & 1) == 0 && i < gn) {
+              const __half hv = __float2half_rn(silu_f(v) * up);
+              bad |= __hisinf(hv) || __hisnan(hv);
+              *(__half *)(hbase + (size_t)i * 128 + (((j >> 3) ^ (i & 7)) << 4) + (j & 7) * 2) = hv;
+            }
+          }
+        }
+        if (bad) record_status(a.ctrl, MOE_ERR_NUMERIC, where);
+      } else {
+        const float s = ((const float *)(it.ebase + L.sd_off))[it.mt * 128 + r];
+        const long yrow0 = it.sh ? (long)a.T * a.k + it.g.pos0 : (long)it.g.pos0;
+        float *ycol = a.y + yrow0 * a.H + it.mt * 128 + r;
+        for (int c0 = 0; c0 < it.Npad; c0 += 16) {
+          float acc[16];
+          load_sum(c0, acc);
+#pragma unroll
+          for (int jj = 0; jj < 16; jj++)
+            if (c0 + jj < gn) ycol[(size_t)(c0 + jj) * a.H] = acc[jj] * s;
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->acc_empty);
+    }
+    if (!ok && lane == 0) give_up();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc<512>(tbase);
+}
+
+// x -> the gate/up B tiles: per group, [k-chunk][rows rounded up to 8][128-byte swizzled
+// row] of bf16, row = token * P + piece (fp32 x is split into bf16 hi + lo pieces); the
+// padding rows are zero.
+__global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, int is_bf16,
+                                                       const int32_t *perm) {
+  const int gi = blockIdx.x;
+  if (gi >= a.ctrl->n_groups) return;
+  const Group g = a.groups[gi];
+  const bool sh = g.e == a.E;
+  const int rows = a.P * g.n, rows8 = round8(rows), KC = a.H / kKChunk;
+  uint8_t *base = const_cast<uint8_t *>(a.xg) + (size_t)g.xrow0 * a.H * 2;
+  for (int idx = threadIdx.x; idx < KC * rows8 * 8; idx += blockDim.x) {
+    const int c = idx & 7, row = (idx >> 3) % rows8, kc = idx / (8 * rows8);
+    uint4 *dst = (uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4));
+    if (row >= rows) { *dst = make_uint4(0, 0, 0, 0); continue; }
+    const int i = row / a.P, piece = row % a.P;
+    const int tok = sh ? g.pos0 + i : perm[g.pos0 + i] / a.k;
+    const size_t col = (size_t)kc * kKChunk + c * 8;
+    if (is_bf16) {
+      *dst = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
+    } else {
+      const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
+      float4 f0 = src[0], f1 = src[1];
+      float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        __nv_bfloat162 hi = __floats2bfloat162_rn(f[2 * m], f[2 * m + 1]);
+        __nv_bfloat162 v = hi;
+        if (piece)
+          v = __floats2bfloat162_rn(f[2 * m] - __low2float(hi), f[2 * m + 1] - __high2float(hi));
+        o[m] = *(uint32_t *)&v;
+      }
+      *dst = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+template <int BITS, bool DOWN, int NMAX>
+static int launch_tc(const TcArgs &a, int bound, int sms, cudaStream_t st) {
+  auto k = tc_expert_kernel<BITS, DOWN, NMAX>;
+  constexpr size_t smem = tc_smem<NMAX>();
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k<<<bound < sms ? bound : sms, kThreads, smem, st>>>(a, bound);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// NMAX: the smallest supported width >= the largest B row count of any group in the launch
+template <int BITS, bool DOWN>
+static int launch_tc_n(TcArgs a, int rows_max, int kc_gcd, int bound, int sms, cudaStream_t st) {
+  // chunks per copy: code runs of 4 chunks (16 KB at int4) where every K allows it;
+  // activation tiles in runs too when they are small (decode), else one chunk per copy
+  a.ra = kc_gcd % 4 == 0 ? 4 : (kc_gcd % 2 == 0 ? 2 : 1);
+  a.rb = rows_max <= 32 ? a.ra : 1;
+  if (rows_max <= 16) return launch_tc<BITS, DOWN, 16>(a, bound, sms, st);
+  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32>(a, bound, sms, st);
+  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64>(a, bound, sms, st);
+  return launch_tc<BITS, DOWN, 128>(a, bound, sms, st);
+}
+
+static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
+
+template <int BITS>
+static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16,
+                  const int32_t *perm, cudaStream_t st, void *mid) {
+  DevInfo d = dev_info();
+  if ((long)tc_smem<128>() > d.smem_optin || (long)tc_smem<16>() > d.smem_optin ||
+      (long)mma_smem_bytes(BITS) > d.smem_optin)
+    return MOE_ERR_UNSUPPORTED;
+  gather_x_kernel<<<W.max_groups, 256, 0, st>>>(a, x, is_bf16, perm);
+  const int mt_s = a.LS.inter / 64, mt_r = a.LR.inter / 64, mt_d = a.H / 128;
+  const int bound_gu = a.ns * mt_s + (W.max_groups - a.ns) * mt_r;
+  const int bound_dn = W.max_groups * mt_d;
+  // a group holds at most min(group_n, T) tokens (a token takes an expert at most once)
+  const int grows = W.group_n < a.T ? W.group_n : a.T;
+  // groups of at most 16 B rows (decode) take the register-MMA kernel, larger ones the
+  // tensor-memory kernel
+  const int rows_gu = a.P * grows;
+  int r = rows_gu <= kMmaMaxRows
+              ? launch_experts_mma(BITS, false, a, rows_gu, a.H / kKChunk, bound_gu, d.sms, st)
+              : launch_tc_n<BITS, false>(a, rows_gu, a.H / kKChunk, bound_gu, d.sms, st);
+  if (r) return r;
+  if (mid && cudaEventRecord((cudaEvent_t)mid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  TcArgs ad = a;
+  ad.trace = nullptr;  // traces (development builds) cover the gate/up kernel
+  const int kc_dn = gcd_i(a.LR.inter / kKChunk, a.LS.inter / kKChunk);
+  return grows <= kMmaMaxRows
+             ? launch_experts_mma(BITS, true, ad, grows, kc_dn, bound_dn, d.sms, st)
+             : launch_tc_n<BITS, true>(ad, grows, kc_dn, bound_dn, d.sms, st);
+}
+
+int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const void *x,
+                      moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
+                      void *mid) {
+  PackLayout P = pack_layout(c);
+  TcArgs a{};
+  a.routed = packed + P.experts_off;
+  a.routed_stride = P.routed.bytes;
+  a.shared = c.n_shared ? packed + P.shared_off : nullptr;
+  a.LR = P.routed;
+  a.LS = P.shared;
+  a.H = c.hidden;
+  a.E = c.n_experts;
+  a.k = c.top_k;
+  a.T = T;
+  int Is = c.inter_shared ? c.inter_shared : c.inter;
+  a.Imax = c.inter > Is ? c.inter : Is;
+  a.P = W.pieces;
+  a.groups = (const Group *)(ws + W.groups);
+  a.ctrl = (Ctrl *)(ws + W.ctrl);
+  a.ns = c.n_shared ? (T + W.group_n - 1) / W.group_n : 0;
+  a.xg = ws + W.xg;
+  a.hg = ws + W.hg;
+  a.y = (float *)(ws + W.y);
+  a.wait_limit = 2000000000L;  // 2 s: a wait this long means the pipeline is stuck
+#ifdef MOE_TRACE
+  a.trace = g_trace;
+#endif
+  const int32_t *perm = (const int32_t *)(ws + W.perm);
+  const int is_bf16 = dt == MOE_DT_BF16;
+  switch (c.weight_bits) {
+    case 4: return run_tc<4>(a, W, x, is_bf16, perm, st, mid);
+    case 2: return run_tc<2>(a, W, x, is_bf16, perm, st, mid);
+    case 8: return run_tc<8>(a, W, x, is_bf16, perm, st, mid);
+    default: return MOE_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace moe

@@ -194,7 +194,7 @@ static int common_args(const moe_layer_config *cfg, const void *packed, const vo
   if (!aligned(packed, 256) || !aligned(ws, 256) || !aligned(x, 16) || !aligned(ids, 4) ||
       !aligned(w, 4))
     return MOE_ERR_INVALID_ARG;
-  *W = ws_layout(*cfg, T);
+  *W = ws_layout(*cfg, T, dt == MOE_DT_F32 ? 2 : 1);
   if (ws_bytes < W->total) return MOE_ERR_WORKSPACE;
   if (!tokens_supported(*cfg, T)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -255,8 +255,9 @@ int moe_forward_launches(const moe_layer_config *cfg, int T) {
   int r = check(cfg);
   if (r) return r;
   if (T <= 0) return 0;
-  // router logits + top-k, permute, [Q8_0 encode], gate/up, down, combine
-  return 2 + 1 + (cfg->act_q8_0 ? 1 : 0) + 2 + 1;
+  // router logits + top-k, permute, [Q8_0 encode], [activation tile gather], gate/up,
+  // down, combine
+  return 2 + 1 + (cfg->act_q8_0 ? 1 : 0) + (use_tc(*cfg) ? 1 : 0) + 2 + 1;
 }
 
 int moe_read_status(void *ws, void *stream) {

@@ -80,45 +80,65 @@ static inline PackLayout pack_layout(const moe_layer_config &c) {
 
 // ---------------------------------------------------------------- workspace
 // [ctrl 256 B][router partials fp32 HS*T*E][offsets E+1][perm T*k][slot_pos T*k]
-// [groups int4 max_groups][xq int8 T*H][xd fp32 T*H/32][h fp32 R*Imax][y fp32 R*H]
-// with R = T*k + n_shared*T rows (routed slots in permuted order, then shared tokens).
+// [groups max_groups][xq int8 T*H][xd fp32 T*H/32]
+// tensor-core path: [xg bf16 tiles][hg fp16 tiles]   CUDA-core path: [h fp32 R*Imax]
+// [y fp32 R*H], with R = T*k + n_shared*T rows (routed slots in permuted order, then the
+// shared expert's tokens).  xg / hg hold each group's activation rows as 128-byte-swizzled
+// tiles [k-chunk][rows rounded up to 8][64 elements], the B operand layout of the
+// tensor-core GEMMs (1024-byte aligned chunk tiles).
 struct Ctrl {
   int status;      // moe_status recorded on the device (0 = OK)
   int detail;      // where it was recorded (kernel id)
-  int n_groups;    // routed groups written by the permute kernel
+  int n_groups;    // groups written by the permute kernel (shared groups included)
   int pad[61];
 };
 
-constexpr int kRouterHS = 8;  // H splits of the small-T router GEMV
+constexpr int kRouterHS = 8;   // H splits of the small-T router GEMV
+constexpr int kTcMaxRows = 128;  // B-operand rows (tokens x pieces) of one tensor-core group
+
+// Expert kernels: tcgen05 tensor-core GEMMs for float activations; the CUDA-core dp4a
+// kernels for Q8_0 activations (per-32-block integer dots with per-block scales).
+static inline bool use_tc(const moe_layer_config &c) { return !c.act_q8_0; }
 
 struct WsLayout {
-  uint64_t ctrl, partials, offsets, perm, slot_pos, groups, xq, xd, h, y, total;
-  int max_groups, group_n, rows;
+  uint64_t ctrl, partials, offsets, perm, slot_pos, groups, xq, xd, xg, hg, h, y, total;
+  int max_groups, group_n, rows, pieces;
+  bool tc;
 };
 
 int choose_group_n(const moe_layer_config &c, int T);
 size_t permute_smem(int T, int E);
 
-static inline WsLayout ws_layout(const moe_layer_config &c, int T) {
+// `pieces`: bf16 rows per token in the tensor-core B operand (1 for bf16 x, 2 for fp32 x
+// split as hi + lo).  Region offsets and the total do not depend on it.
+static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 1) {
   WsLayout W;
   int Is = c.inter_shared ? c.inter_shared : c.inter;
   int Imax = c.inter > Is ? c.inter : Is;
   int k = c.top_k;
-  W.group_n = choose_group_n(c, T);
+  W.tc = use_tc(c);
+  W.pieces = pieces;
+  int gn_min = W.tc ? kTcMaxRows / 2 : choose_group_n(c, T);
+  W.group_n = W.tc ? kTcMaxRows / pieces : gn_min;
   W.rows = T * k + (c.n_shared ? T : 0);
   int tk = T * k;
-  W.max_groups = (tk + W.group_n - 1) / W.group_n + (c.n_experts < tk ? c.n_experts : tk) +
-                 (c.n_shared ? (T + W.group_n - 1) / W.group_n : 0) + 1;
+  W.max_groups = (tk + gn_min - 1) / gn_min + (c.n_experts < tk ? c.n_experts : tk) +
+                 (c.n_shared ? (T + gn_min - 1) / gn_min : 0) + 1;
+  // tile rows per group are padded to a multiple of 8: up to 7 extra rows per group
+  uint64_t xg_rows = W.tc ? (uint64_t)2 * W.rows + 7ull * W.max_groups : 0;
+  uint64_t hg_rows = W.tc ? (uint64_t)W.rows + 7ull * W.max_groups : 0;
   uint64_t o = 0;
   W.ctrl = o; o += 256;
   W.partials = o; o = align_up(o + (uint64_t)kRouterHS * T * c.n_experts * 4, 256);
   W.offsets = o; o = align_up(o + (uint64_t)(c.n_experts + 1) * 4, 256);
   W.perm = o; o = align_up(o + (uint64_t)tk * 4, 256);
   W.slot_pos = o; o = align_up(o + (uint64_t)tk * 4, 256);
-  W.groups = o; o = align_up(o + (uint64_t)W.max_groups * 16, 256);
+  W.groups = o; o = align_up(o + (uint64_t)W.max_groups * 32, 256);
   W.xq = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * c.hidden : 0), 256);
-  W.xd = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * (c.hidden / 32) * 4 : 0), 256);
-  W.h = o; o = align_up(o + (uint64_t)W.rows * Imax * 4, 256);
+  W.xd = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * (c.hidden / 32) * 4 : 0), 1024);
+  W.xg = o; o = align_up(o + xg_rows * c.hidden * 2, 1024);
+  W.hg = o; o = align_up(o + hg_rows * Imax * 2, 256);
+  W.h = o; o = align_up(o + (W.tc ? 0 : (uint64_t)W.rows * Imax * 4), 256);
   W.y = o; o = align_up(o + (uint64_t)W.rows * c.hidden * 4, 256);
   W.total = o;
   return W;
@@ -132,11 +152,15 @@ __device__ __forceinline__ void record_status(Ctrl *ctrl, int status, int where)
   if (atomicCAS(&ctrl->status, 0, status) == 0) ctrl->detail = where;
 }
 
-// A routed group: `n` permuted rows starting at `pos0` that all use expert `e`.
-// For the shared expert (e == E), rows are tokens pos0 .. pos0+n-1.
+// A group: `n` permuted rows starting at `pos0` that all use expert `e`.  For the shared
+// expert (e == E), rows are tokens pos0 .. pos0+n-1.  xrow0 / hrow0: the group's first
+// row in the xg / hg tile buffers (tensor-core path).
 struct Group {
-  int e, pos0, n, pad;
+  int e, pos0, n, xrow0, hrow0, pad0, pad1, pad2;
 };
+
+__host__ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
+__host__ __device__ __forceinline__ int round8(int v) { return (v + 7) & ~7; }
 
 // ---------------------------------------------------------------- launch helpers
 struct DevInfo {
@@ -153,6 +177,9 @@ int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t
                    const WsLayout &W, cudaStream_t st);
 int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
+int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const void *x,
+                      moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
+                      void *mid);
 // mid_event (a cudaEvent_t or null) is recorded between the gate/up and down launches
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,

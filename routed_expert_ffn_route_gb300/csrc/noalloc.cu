@@ -8,7 +8,7 @@
 // For them, moe_layer_forward_static runs the same kernels as moe_layer_forward, with the
 // scratch in a file-scope device array instead of a caller buffer.
 //
-// The array (kStaticScratchBytes, 8 MiB) is part of the library image: every GPU that
+// The array (kStaticScratchBytes, 32 MiB) is part of the library image: every GPU that
 // loads the library holds it until the process exits.  In host code `g_scratch` names a
 // host-side stand-in, not a device address, so the device address is looked up with
 // cudaGetSymbolAddress once per device, with that device current, on the first call
@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = (size_t)8 << 20;
+constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
 
 __device__ __align__(256) unsigned char g_scratch[kStaticScratchBytes];
 

@@ -5,29 +5,33 @@
 // One CTA of 1024 threads:
 //  1. per 32-token chunk, a bitmask per expert of the chunk's tokens that chose it
 //     (shared-memory atomicOr), giving per-chunk per-expert counts;
-//  2. exclusive scans: per-expert offsets (expert_offsets), per-expert chunk bases;
+//  2. exclusive scans: per-expert offsets (expert_offsets), per-expert chunk bases, and
+//     the work-list positions (first group of each expert);
 //  3. stable scatter: the rank of slot (t, j) inside expert e is its chunk base plus
 //     popc(mask & lanes-below), so perm lists t*k+j ordered by (expert, token) exactly,
 //     without any order decided by atomics;
 //  4. the work list of the expert kernels: groups of at most GN rows of one expert
-//     (shared-expert groups first, over the tokens in order).
+//     (shared-expert groups first, over the tokens in order), each with its first row in
+//     the tensor-core activation tiles (row index + 7 x group index: room to pad each
+//     group's rows to a multiple of 8).
 #include "dev.cuh"
 #include "moe_internal.cuh"
 
 namespace moe {
 
-// shared memory: masks [32][E] u32 | chunk bases [n_chunks][E] u16 | offs [E+1] | gstart [E+1]
+// shared memory: masks [32][E] u32 | chunk bases [n_chunks][E] u16 | 2 x [E+1] int
 __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int n_shared, int GN,
-                                                       const int32_t *ids, int32_t *offsets_out,
-                                                       int32_t *perm, int32_t *slot_pos,
-                                                       Group *groups, Ctrl *ctrl) {
+                                                       int P, const int32_t *ids,
+                                                       int32_t *offsets_out, int32_t *perm,
+                                                       int32_t *slot_pos, Group *groups,
+                                                       Ctrl *ctrl) {
   extern __shared__ uint32_t sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_chunks = (T + 31) / 32;
   uint32_t *masks = sm;                                    // [32][E]
   uint16_t *cbase = (uint16_t *)(sm + 32 * E);             // [n_chunks][E]
-  int *offs = (int *)(cbase + ((n_chunks * E + 1) & ~1));  // [E+1]
-  int *gstart = offs + (E + 1);                            // [E+1]
+  int *offs = (int *)(cbase + ((n_chunks * E + 1) & ~1));  // [E+1] token offsets
+  int *gstart = offs + (E + 1);                            // [E+1] first group
   uint32_t *my = masks + warp * E;
 
   // 1. per-chunk per-expert counts
@@ -50,42 +54,46 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
       cbase[c * E + e] = (uint16_t)run;
       run += v;
     }
-    offs[e] = run;                          // count for now
-    gstart[e] = (run + GN - 1) / GN;        // groups of this expert
+    offs[e] = run;                    // counts for now
+    gstart[e] = (run + GN - 1) / GN;  // groups of this expert
   }
   __syncthreads();
-  // 2b. exclusive scans of counts and group counts (one warp, E <= 256)
+  // 2b. exclusive scans of the per-expert counts and group counts (one warp, E <= 256)
   if (warp == 0) {
+    int *arr[2] = {offs, gstart};
     int per = (E + 31) / 32;
-    int s0 = 0, s1 = 0;
+    int s[2] = {0, 0};
     for (int i = 0; i < per; i++) {
       int e = lane * per + i;
-      if (e < E) { s0 += offs[e]; s1 += gstart[e]; }
+      if (e < E)
+        for (int q = 0; q < 2; q++) s[q] += arr[q][e];
     }
-    int i0 = s0, i1 = s1;
+    int inc[2];
+    for (int q = 0; q < 2; q++) {
+      inc[q] = s[q];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int a = __shfl_up_sync(0xffffffffu, i0, o), b = __shfl_up_sync(0xffffffffu, i1, o);
-      if (lane >= o) { i0 += a; i1 += b; }
-    }
-    int r0 = i0 - s0, r1 = i1 - s1;  // exclusive
-    for (int i = 0; i < per; i++) {
-      int e = lane * per + i;
-      if (e < E) {
-        int c0 = offs[e], c1 = gstart[e];
-        offs[e] = r0;
-        gstart[e] = r1;
-        r0 += c0;
-        r1 += c1;
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, inc[q], o);
+        if (lane >= o) inc[q] += v;
       }
     }
-    if (lane == 31) {
-      offs[E] = i0;
-      gstart[E] = i1;
+    int r[2];
+    for (int q = 0; q < 2; q++) r[q] = inc[q] - s[q];
+    for (int i = 0; i < per; i++) {
+      int e = lane * per + i;
+      if (e < E)
+        for (int q = 0; q < 2; q++) {
+          int v = arr[q][e];
+          arr[q][e] = r[q];
+          r[q] += v;
+        }
     }
+    if (lane == 31)
+      for (int q = 0; q < 2; q++) arr[q][E] = inc[q];
   }
   __syncthreads();
   const int ns = n_shared ? (T + GN - 1) / GN : 0;
+  const int rbase = n_shared ? T : 0;  // routed rows follow the shared expert's T rows
   if (threadIdx.x == 0) ctrl->n_groups = ns + gstart[E];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets_out[e] = offs[e];
   // 3. stable scatter
@@ -109,12 +117,14 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
   }
   // 4. groups
   for (int i = threadIdx.x; i < ns; i += blockDim.x)
-    groups[i] = Group{E, i * GN, min(GN, T - i * GN), 0};
+    groups[i] = Group{E, i * GN, min(GN, T - i * GN), P * i * GN + 7 * i, i * GN + 7 * i, 0, 0, 0};
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int n = offs[e + 1] - offs[e];
     int g0 = ns + gstart[e];
     for (int g = 0; g * GN < n; g++)
-      groups[g0 + g] = Group{e, offs[e] + g * GN, min(GN, n - g * GN), 0};
+      groups[g0 + g] = Group{e, offs[e] + g * GN, min(GN, n - g * GN),
+                             P * (rbase + offs[e] + g * GN) + 7 * (g0 + g),
+                             rbase + offs[e] + g * GN + 7 * (g0 + g), 0, 0, 0};
   }
 }
 
@@ -131,7 +141,7 @@ int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   permute_kernel<<<1, 1024, smem, st>>>(
-      T, c.top_k, c.n_experts, c.n_shared, W.group_n, ids, (int32_t *)(ws + W.offsets),
+      T, c.top_k, c.n_experts, c.n_shared, W.group_n, W.pieces, ids, (int32_t *)(ws + W.offsets),
       (int32_t *)(ws + W.perm), (int32_t *)(ws + W.slot_pos), (Group *)(ws + W.groups),
       (Ctrl *)(ws + W.ctrl));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

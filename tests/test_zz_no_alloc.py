@@ -3,7 +3,7 @@
 For callers that cannot give the library device scratch (an operator plugin that only
 receives its input and output tensors, a serving loop that forbids allocation after
 start-up, code that must not call cudaMalloc because it may synchronise the device), the
-library keeps its scratch in its own 8 MiB device array.  This test calls that entry
+library keeps its scratch in its own 32 MiB device array.  This test calls that entry
 point through the C ABI twice in a row and checks each result against moe_layer_forward
 with a caller workspace, within the parity tolerance of the other tests.  It builds its
 own layer, so it passes alone in a fresh process as well as after the other tests; the
@@ -63,8 +63,8 @@ def test_static_scratch_forward_matches_workspace_forward(spec, T):
 def test_static_scratch_rejects_oversized_calls():
     s = gen.spec("dsv3")
     cfg = gen.device.config_for(s)
-    T = 64  # its workspace is far above the 8 MiB array
-    assert moe.moe_workspace_bytes(cfg, T) > (8 << 20)
+    T = 64  # its workspace is far above the 32 MiB array
+    assert moe.moe_workspace_bytes(cfg, T) > (32 << 20)
     r = moe.lib().moe_layer_forward_static(
         C.byref(cfg), C.c_void_p(256), C.c_void_p(256), moe.MOE_DT_BF16, T, C.c_void_p(256),
         C.c_void_p(256), C.c_void_p(256), None, None)
