@@ -23,7 +23,8 @@ struct TcArgs {
   const Group *groups;
   Ctrl *ctrl;
   int ns;
-  const uint8_t *xg;  // gate/up B tiles (bf16)
+  const uint8_t *xg;  // gate/up B tiles (fp16, x_t * tscale[t])
+  float *rscale;      // per xg row: 1 / tscale of the row's token
   uint8_t *hg;        // gate/up output = down B tiles (fp16)
   float *y;           // down output [rows][H]
   int ra, rb;         // chunks per code run / per activation-tile run
@@ -87,6 +88,65 @@ __device__ __forceinline__ bool wait_nofail(uint64_t *bar, uint32_t parity, long
   while (!tc::mbar_try_wait_sleep(bar, parity, 20000))
     if ((long)(tc::global_ns() - t0) > limit_ns) return false;
   return true;
+}
+
+// ---------------------------------------------------------------- codes -> fp16 pairs
+// Dequantisation to exact small integers in fp16 (the codes' per-row scale is applied to
+// the fp32 accumulator).  A biased code c placed in the low mantissa bits of 1024.0
+// (0x6400) reads as 1024 + c; placed 4 (or 2, 6) bits higher it reads as 1024 + 16c
+// (4c, 64c), and one fused multiply-add by 1/16 (1/4, 1/64) removes both the magic and
+// the bias.  Every intermediate is an integer below 2048 or its exact power-of-two
+// multiple, so each step is exact.  The pair of a word's two 16-bit halves is one (lo, hi)
+// fragment register of a 16-bit MMA operand.
+__device__ __forceinline__ uint32_t h2_sub(uint32_t v, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t v, uint32_t m, uint32_t a) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(m), "r"(a));
+  return r;
+}
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t v, uint32_t mask, uint32_t magic) {
+  uint32_t r;  // (v & mask) | magic in one logic op: truth table (a & b) | c = 0xEA
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(mask), "r"(magic));
+  return r;
+}
+
+// int4 word (pair p in nibbles p and p+4) -> pairs 0..3
+__device__ __forceinline__ void dq_word_i4(uint32_t w, uint32_t *o) {
+  const uint32_t M = 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  o[0] = h2_sub(lop_and_or(w, 0x000F000Fu, M), 0x64086408u);               // 1024+c - 1032
+  o[1] = h2_fma(lop_and_or(w, 0x00F000F0u, M), 0x2C002C00u, 0xD480D480u);  // /16 - 72
+  o[2] = h2_sub(lop_and_or(w8, 0x000F000Fu, M), 0x64086408u);
+  o[3] = h2_fma(lop_and_or(w8, 0x00F000F0u, M), 0x2C002C00u, 0xD480D480u);
+}
+
+// int2 word (pair p in 2-bit fields p and p+8) -> pairs 0..7
+__device__ __forceinline__ void dq_word_i2(uint32_t w, uint32_t *o) {
+  const uint32_t M = 0x64006400u;
+#pragma unroll
+  for (int half = 0; half < 2; half++) {
+    const uint32_t v = half ? w >> 8 : w;
+    uint32_t *q = o + 4 * half;
+    q[0] = h2_sub(lop_and_or(v, 0x00030003u, M), 0x64026402u);               // 1024+c - 1026
+    q[1] = h2_fma(lop_and_or(v, 0x000C000Cu, M), 0x34003400u, 0xDC08DC08u);  // /4 - 258
+    q[2] = h2_fma(lop_and_or(v, 0x00300030u, M), 0x2C002C00u, 0xD420D420u);  // /16 - 66
+    q[3] = h2_fma(lop_and_or(v, 0x00C000C0u, M), 0x24002400u, 0xCC80CC80u);  // /64 - 18
+  }
+}
+
+// int8 word (two's complement bytes 0..3) -> pairs 0..1: b ^ 0x80 = b + 128 in [0, 255]
+// goes under 0x64 (1024 + b + 128), minus 1152
+__device__ __forceinline__ void dq_word_i8(uint32_t w, uint32_t *o) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  o[0] = h2_sub(a, 0x64806480u);
+  o[1] = h2_sub(b, 0x64806480u);
 }
 
 // Small-group expert GEMMs (every group's B rows <= kMmaMaxRows): register-MMA kernel.

@@ -29,6 +29,8 @@
 // issuers' accumulators, scale, SwiGLU, stores).  Every wait is bounded: a wait that gives up
 // records MOE_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained and TMEM
 // is freed before exit.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -99,68 +101,30 @@ constexpr size_t tc_smem() {
   return 1024 + (size_t)Plan<NMAX>::a_ring + Plan<NMAX>::b_ring + sizeof(TcBars);
 }
 
-__device__ __forceinline__ uint32_t sub_bf16x2(uint32_t v, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t sub_f16x2(uint32_t v, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(b));
-  return r;
-}
-
-// One weight row's 64 codes (one k-chunk) -> 32 pairs of exact 16-bit integers (element
-// 2c in the low half of column c).  F16: fp16 pairs (down); else bf16 pairs (gate/up).
-// Rows are 32 B apart at int4: lanes read the two 16-byte halves in an order that puts
-// the 8 lanes of each shared-memory phase on distinct banks.
-template <int BITS, bool F16>
+// One weight row's 64 codes (one k-chunk) -> 32 pairs of exact fp16 integers (element 2c
+// in the low half of column c).  Rows are 32 B apart at int4: lanes read the two 16-byte
+// halves in an order that puts the 8 lanes of each shared-memory phase on distinct banks.
+template <int BITS>
 __device__ __forceinline__ void dequant_row(const uint8_t *src, int lane, uint32_t (&o)[32]) {
   if (BITS == 4) {
-    const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;  // 1024 / 128 in both halves
-    const uint32_t bias = F16 ? 0x64086408u : 0x43084308u;   // 1032 / 136: magic + 8
     const int h0 = (lane >> 2) & 1;
     const uint4 ua = ((const uint4 *)src)[h0], ub = ((const uint4 *)src)[h0 ^ 1];
     const uint4 u0 = h0 ? ub : ua, u1 = h0 ? ua : ub;
-    uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-    for (int i = 0; i < 8; i++)
-#pragma unroll
-      for (int p = 0; p < 4; p++) {
-        uint32_t v = ((w[i] >> (4 * p)) & 0x000F000Fu) | magic;
-        o[4 * i + p] = F16 ? sub_f16x2(v, bias) : sub_bf16x2(v, bias);
-      }
+    for (int i = 0; i < 8; i++) dq_word_i4(w[i], o + 4 * i);
   } else if (BITS == 2) {
-    const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;
-    const uint32_t bias = F16 ? 0x64026402u : 0x43024302u;  // magic + 2
-    uint4 u0 = ((const uint4 *)src)[0];
-    uint32_t w[4] = {u0.x, u0.y, u0.z, u0.w};
+    const uint4 u = ((const uint4 *)src)[0];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int i = 0; i < 4; i++)
-#pragma unroll
-      for (int p = 0; p < 8; p++) {
-        uint32_t v = ((w[i] >> (2 * p)) & 0x00030003u) | magic;
-        o[8 * i + p] = F16 ? sub_f16x2(v, bias) : sub_bf16x2(v, bias);
-      }
+    for (int i = 0; i < 4; i++) dq_word_i2(w[i], o + 8 * i);
   } else {
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-      uint4 u = ((const uint4 *)src)[q];
-      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      const uint4 u = ((const uint4 *)src)[q];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        float f0 = (float)(int8_t)(w[i] & 0xFF), f1 = (float)(int8_t)((w[i] >> 8) & 0xFF);
-        float f2 = (float)(int8_t)((w[i] >> 16) & 0xFF), f3 = (float)(int8_t)(w[i] >> 24);
-        if (F16) {
-          __half2 a = __floats2half2_rn(f0, f1), b = __floats2half2_rn(f2, f3);
-          o[8 * q + 2 * i] = *(uint32_t *)&a;
-          o[8 * q + 2 * i + 1] = *(uint32_t *)&b;
-        } else {
-          __nv_bfloat162 a = __floats2bfloat162_rn(f0, f1), b = __floats2bfloat162_rn(f2, f3);
-          o[8 * q + 2 * i] = *(uint32_t *)&a;
-          o[8 * q + 2 * i + 1] = *(uint32_t *)&b;
-        }
-      }
+      for (int i = 0; i < 4; i++) dq_word_i8(w[i], o + 8 * q + 2 * i);
     }
   }
 }
@@ -171,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   constexpr int ST = PL::stages, NI = PL::issuers;
   constexpr int AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
   extern __shared__ uint8_t smraw[];
-  uint8_t *base = (uint8_t *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint8_t *base = tc::align_smem_1024(smraw);
   uint8_t *bring = base;
   uint8_t *aring = base + PL::b_ring;
   TcBars *bars = (TcBars *)(aring + PL::a_ring);
@@ -262,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         if (!tc_item<DOWN>(a, item, it)) break;
         if (!tc::mbar_wait(&bars->acc_empty, (n & 1) ^ 1, abort, lim)) { ok = false; break; }
         tc::fence_after_sync();
-        const uint32_t idesc = tc::idesc_f16(DOWN ? 0 : 1, it.Npad);
+        const uint32_t idesc = tc::idesc_f16(0, it.Npad);  // fp16 x fp16 -> fp32
         const uint32_t dcol = tbase + PL::acc_col + me * NMAX;
         bool first = true;
         for (int kc = 0; kc < it.KC; kc++, c++) {
@@ -314,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         if (!ok) break;
         if (r == 0) MOE_TC_TRACE(2, c);
         uint32_t v[32];
-        dequant_row<BITS, DOWN>(aring + sa * a_run + (c % ra) * AB + r * RB, lane, v);
+        dequant_row<BITS>(aring + sa * a_run + (c % ra) * AB + r * RB, lane, v);
         tc::mbar_arrive(&bars->a_empty[sa]);
         ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[st], pt ^ 1, abort, lim));
         if (!ok) break;
@@ -355,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       const int gn = it.g.n;
       if (!DOWN) {
         const float s = ((const float *)(it.ebase + L.sgu_off))[it.mt * 128 + r];
+        const float *rsc = a.rscale + it.g.xrow0;  // 1 / the token's activation scale
         const int j = r >> 1;  // output index within the m-tile (64 outputs)
         uint8_t *hbase =
             a.hg + (size_t)it.g.hrow0 * a.Imax * 2 + (size_t)it.mt * round8(gn) * 128;
@@ -367,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
             if (a.P == 2 && (jj & 1)) continue;  // the lo piece, folded into its hi column
             float v = acc[jj];
             if (a.P == 2) v += acc[(jj + 1) & 15];
-            v *= s;
+            v *= s * (c0 + jj < it.rowsB ? rsc[c0 + jj] : 0.f);
             const float up = __shfl_xor_sync(0xffffffffu, v, 1);
             const int i = (c0 + jj) / a.P;  // token within the group
             if ((r & 1) == 0 && i < gn) {
@@ -402,40 +367,53 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
 }
 
 // x -> the gate/up B tiles: per group, [k-chunk][rows rounded up to 8][128-byte swizzled
-// row] of bf16, row = token * P + piece (fp32 x is split into bf16 hi + lo pieces); the
-// padding rows are zero.
+// row] of fp16 x_t * tscale[t], row = token * P + piece (fp32 x is split into fp16 hi + lo
+// pieces); the padding rows are zero.  Also rscale[row] = 1 / tscale of the row's token.
+// blockIdx.x: group; blockIdx.y strides over the group's (chunk, row, 16-byte) units.
 __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, int is_bf16,
-                                                       const int32_t *perm) {
+                                                       const int32_t *perm, const float *tscale) {
   const int gi = blockIdx.x;
   if (gi >= a.ctrl->n_groups) return;
   const Group g = a.groups[gi];
   const bool sh = g.e == a.E;
   const int rows = a.P * g.n, rows8 = round8(rows), KC = a.H / kKChunk;
   uint8_t *base = const_cast<uint8_t *>(a.xg) + (size_t)g.xrow0 * a.H * 2;
-  for (int idx = threadIdx.x; idx < KC * rows8 * 8; idx += blockDim.x) {
+  auto token = [&](int row) { return sh ? g.pos0 + row / a.P : perm[g.pos0 + row / a.P] / a.k; };
+  if (blockIdx.y == 0)
+    for (int row = threadIdx.x; row < rows8; row += blockDim.x)
+      a.rscale[g.xrow0 + row] = row < rows ? 1.0f / tscale[token(row)] : 0.f;
+  const int units = KC * rows8 * 8;
+  for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < units; idx += gridDim.y * blockDim.x) {
     const int c = idx & 7, row = (idx >> 3) % rows8, kc = idx / (8 * rows8);
     uint4 *dst = (uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4));
     if (row >= rows) { *dst = make_uint4(0, 0, 0, 0); continue; }
-    const int i = row / a.P, piece = row % a.P;
-    const int tok = sh ? g.pos0 + i : perm[g.pos0 + i] / a.k;
+    const int tok = token(row), piece = row % a.P;
+    const float sc = tscale[tok];
     const size_t col = (size_t)kc * kKChunk + c * 8;
+    float f[8];
     if (is_bf16) {
-      *dst = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
-    } else {
-      const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
-      float4 f0 = src[0], f1 = src[1];
-      float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-      uint32_t o[4];
+      const uint4 u = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
+      const uint32_t q[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int m = 0; m < 4; m++) {
-        __nv_bfloat162 hi = __floats2bfloat162_rn(f[2 * m], f[2 * m + 1]);
-        __nv_bfloat162 v = hi;
-        if (piece)
-          v = __floats2bfloat162_rn(f[2 * m] - __low2float(hi), f[2 * m + 1] - __high2float(hi));
-        o[m] = *(uint32_t *)&v;
+        f[2 * m] = __uint_as_float(q[m] << 16);
+        f[2 * m + 1] = __uint_as_float(q[m] & 0xFFFF0000u);
       }
-      *dst = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
+      const float4 f0 = src[0], f1 = src[1];
+      f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
+      f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
     }
+    uint32_t o[4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+      const float v0 = f[2 * m] * sc, v1 = f[2 * m + 1] * sc;  // exact: sc is a power of two
+      __half2 hv = __floats2half2_rn(v0, v1);
+      if (piece) hv = __floats2half2_rn(v0 - __low2float(hv), v1 - __high2float(hv));
+      o[m] = *(uint32_t *)&hv;
+    }
+    *dst = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -465,12 +443,14 @@ static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
 
 template <int BITS>
 static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16,
-                  const int32_t *perm, cudaStream_t st, void *mid) {
+                  const int32_t *perm, const float *tscale, cudaStream_t st, void *mid) {
   DevInfo d = dev_info();
   if ((long)tc_smem<128>() > d.smem_optin || (long)tc_smem<16>() > d.smem_optin ||
       (long)mma_smem_bytes(BITS) > d.smem_optin)
     return MOE_ERR_UNSUPPORTED;
-  gather_x_kernel<<<W.max_groups, 256, 0, st>>>(a, x, is_bf16, perm);
+  // enough CTAs to cover the SMs a few times over, whatever the group count
+  const int gy = std::max(1, std::min(a.H / kKChunk, (4 * d.sms + W.max_groups - 1) / W.max_groups));
+  gather_x_kernel<<<dim3(W.max_groups, gy), 256, 0, st>>>(a, x, is_bf16, perm, tscale);
   const int mt_s = a.LS.inter / 64, mt_r = a.LR.inter / 64, mt_d = a.H / 128;
   const int bound_gu = a.ns * mt_s + (W.max_groups - a.ns) * mt_r;
   const int bound_dn = W.max_groups * mt_d;
@@ -513,6 +493,8 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   a.ctrl = (Ctrl *)(ws + W.ctrl);
   a.ns = c.n_shared ? (T + W.group_n - 1) / W.group_n : 0;
   a.xg = ws + W.xg;
+  a.rscale = (float *)(ws + W.rscale);
+  const float *tscale = (const float *)(ws + W.tscale);
   a.hg = ws + W.hg;
   a.y = (float *)(ws + W.y);
   a.wait_limit = 2000000000L;  // 2 s: a wait this long means the pipeline is stuck
@@ -522,9 +504,9 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   const int32_t *perm = (const int32_t *)(ws + W.perm);
   const int is_bf16 = dt == MOE_DT_BF16;
   switch (c.weight_bits) {
-    case 4: return run_tc<4>(a, W, x, is_bf16, perm, st, mid);
-    case 2: return run_tc<2>(a, W, x, is_bf16, perm, st, mid);
-    case 8: return run_tc<8>(a, W, x, is_bf16, perm, st, mid);
+    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, mid);
+    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, mid);
+    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, mid);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

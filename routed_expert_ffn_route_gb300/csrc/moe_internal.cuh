@@ -81,11 +81,14 @@ static inline PackLayout pack_layout(const moe_layer_config &c) {
 // ---------------------------------------------------------------- workspace
 // [ctrl 256 B][router partials fp32 HS*T*E][offsets E+1][perm T*k][slot_pos T*k]
 // [groups max_groups][xq int8 T*H][xd fp32 T*H/32]
-// tensor-core path: [xg bf16 tiles][hg fp16 tiles]   CUDA-core path: [h fp32 R*Imax]
+// tensor-core path: [tscale fp32 T][rscale fp32 xg rows][xg fp16 tiles][hg fp16 tiles]
+// CUDA-core path: [h fp32 R*Imax]
 // [y fp32 R*H], with R = T*k + n_shared*T rows (routed slots in permuted order, then the
 // shared expert's tokens).  xg / hg hold each group's activation rows as 128-byte-swizzled
 // tiles [k-chunk][rows rounded up to 8][64 elements], the B operand layout of the
-// tensor-core GEMMs (1024-byte aligned chunk tiles).
+// tensor-core GEMMs (1024-byte aligned chunk tiles).  xg holds x_t * tscale[t]: tscale is
+// a power of two per token that brings max |x_t| into [2^14, 2^15), so that the fp16
+// operand keeps every bf16 value exactly; rscale[row] = 1 / tscale of the row's token.
 struct Ctrl {
   int status;      // moe_status recorded on the device (0 = OK)
   int detail;      // where it was recorded (kernel id)
@@ -101,7 +104,8 @@ constexpr int kTcMaxRows = 128;  // B-operand rows (tokens x pieces) of one tens
 static inline bool use_tc(const moe_layer_config &c) { return !c.act_q8_0; }
 
 struct WsLayout {
-  uint64_t ctrl, partials, offsets, perm, slot_pos, groups, xq, xd, xg, hg, h, y, total;
+  uint64_t ctrl, partials, offsets, perm, slot_pos, groups, xq, xd, tscale, rscale, xg, hg, h,
+      y, total;
   int max_groups, group_n, rows, pieces;
   bool tc;
 };
@@ -109,7 +113,7 @@ struct WsLayout {
 int choose_group_n(const moe_layer_config &c, int T);
 size_t permute_smem(int T, int E);
 
-// `pieces`: bf16 rows per token in the tensor-core B operand (1 for bf16 x, 2 for fp32 x
+// `pieces`: fp16 rows per token in the tensor-core B operand (1 for bf16 x, 2 for fp32 x
 // split as hi + lo).  Region offsets and the total do not depend on it.
 static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 1) {
   WsLayout W;
@@ -135,7 +139,9 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   W.slot_pos = o; o = align_up(o + (uint64_t)tk * 4, 256);
   W.groups = o; o = align_up(o + (uint64_t)W.max_groups * 32, 256);
   W.xq = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * c.hidden : 0), 256);
-  W.xd = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * (c.hidden / 32) * 4 : 0), 1024);
+  W.xd = o; o = align_up(o + (c.act_q8_0 ? (uint64_t)T * (c.hidden / 32) * 4 : 0), 256);
+  W.tscale = o; o = align_up(o + (W.tc ? (uint64_t)T * 4 : 0), 256);
+  W.rscale = o; o = align_up(o + xg_rows * 4, 1024);
   W.xg = o; o = align_up(o + xg_rows * c.hidden * 2, 1024);
   W.hg = o; o = align_up(o + hg_rows * Imax * 2, 256);
   W.h = o; o = align_up(o + (W.tc ? 0 : (uint64_t)W.rows * Imax * 4), 256);

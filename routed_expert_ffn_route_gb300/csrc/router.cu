@@ -14,6 +14,8 @@
 //    groups are kept; the k largest c of the kept groups are selected; weights are
 //    s / sum(selected s) * routed_scaling_factor.
 // Ties go to the lower index everywhere; slots are in descending selection score.
+// The selection kernel also writes each token's activation scale for the expert GEMMs
+// (a power of two taking max |x_t| into [2^14, 2^15), see token_scale).
 #include "dev.cuh"
 #include "moe_internal.cuh"
 
@@ -148,25 +150,69 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
 
 constexpr int kMaxV = 8;  // experts per lane (E <= 256)
 
+// 2^e with max_abs * 2^e in [2^14, 2^15): x_t * 2^e converts to fp16 without loss for every
+// element that bf16 holds within 2^-24 of the token's largest (fp16 keeps 11 significant
+// bits over that range).  A zero or non-finite maximum gets 1.
+__device__ __forceinline__ float token_scale(float max_abs) {
+  if (!(max_abs > 0.f) || isinf(max_abs)) return 1.f;
+  const int e = (int)((__float_as_uint(max_abs) >> 23) & 0xFF);  // biased exponent
+  int se = 268 - e;  // biased exponent of 2^(141 - e): max_abs in [2^(e-127), 2^(e-126))
+  se = se < 1 ? 1 : (se > 254 ? 254 : se);
+  return __uint_as_float((uint32_t)se << 23);
+}
+
 __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, const float *bias,
                                                           const float *partials, int hsplits,
                                                           int T, int32_t *ids, float *w,
-                                                          Ctrl *ctrl) {
+                                                          Ctrl *ctrl, const void *x, int is_bf16,
+                                                          float *tscale) {
   __shared__ float csm[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const int E = c.n_experts, k = c.top_k;
   const bool grouped = c.router == MOE_ROUTER_SIGMOID_GROUPED;
+  if (tscale) {
+    const int H = c.hidden;
+    float m = 0.f;
+    for (int i = 8 * lane; i < H; i += 256) {
+      if (is_bf16) {
+        const uint4 u = *(const uint4 *)((const uint16_t *)x + (long)t * H + i);
+        const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(q[j] << 16)),
+                             fabsf(__uint_as_float(q[j] & 0xFFFF0000u))));
+      } else {
+        const float4 *f = (const float4 *)((const float *)x + (long)t * H + i);
+        const float4 f0 = f[0], f1 = f[1];
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f0.z), fabsf(f0.w))));
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(f1.x), fabsf(f1.y)), fmaxf(fabsf(f1.z), fabsf(f1.w))));
+      }
+    }
+    m = warp_max(m);
+    if (lane == 0) tscale[t] = token_scale(m);
+  }
   float sel[kMaxV], wsrc[kMaxV];
   float mx = -INFINITY;
+  // the H-split partial logits, all loaded before they are added (in split order)
+  float part[kMaxV][kRouterHS];
+#pragma unroll
+  for (int v = 0; v < kMaxV; v++)
+#pragma unroll
+    for (int hs = 0; hs < kRouterHS; hs++) {
+      const int e = lane + 32 * v;
+      part[v][hs] = (e < E && hs < hsplits) ? partials[((long)hs * T + t) * E + e] : 0.f;
+    }
 #pragma unroll
   for (int v = 0; v < kMaxV; v++) {
     int e = lane + 32 * v;
     float l = -INFINITY;
     if (e < E) {
       l = 0.f;
-      for (int hs = 0; hs < hsplits; hs++) l += partials[((long)hs * T + t) * E + e];
+#pragma unroll
+      for (int hs = 0; hs < kRouterHS; hs++)
+        if (hs < hsplits) l += part[v][hs];
       if (!isfinite(l)) {
         // a non-finite logit: report it, and keep the selection total and in range
         record_status(ctrl, MOE_ERR_NUMERIC, kKTopk);
@@ -286,7 +332,9 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
     router_gemm_kernel<<<grid, 256, 0, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl);
   }
   const float *bias = (const float *)(packed + P.router_b_off);
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(c, bias, partials, hsplits, T, ids, w, ctrl);
+  float *tscale = W.tc ? (float *)(ws + W.tscale) : nullptr;
+  router_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(c, bias, partials, hsplits, T, ids, w, ctrl, x,
+                                                  is_bf16, tscale);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -13,6 +13,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 // ---------------------------------------------------------------- mbarrier
+// `p` rounded up to a 1024-byte shared-memory boundary.  Pointer arithmetic on the shared
+// array itself (no round trip through an integer) keeps the compiler aware that the result
+// is a shared-memory address, so accesses through it stay 32-bit shared loads.
+__device__ __forceinline__ uint8_t *align_smem_1024(uint8_t *p) {
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
