@@ -23,10 +23,10 @@
 // (32 columns each) next to the accumulators.
 //
 // Warp roles: 20 code producer and 21 activation-tile producer (bulk copies, one thread
-// each), 0-3 MMA issuers (one thread each, taking turns by chunk, each into its own TMEM
-// accumulator), 8-19 dequantisers in three sets that take turns by chunk (one weight row
-// per thread, smem -> registers -> TMEM), 4-7 epilogue (TMEM -> registers, sum of the
-// issuers' accumulators, scale, SwiGLU, stores).  Every wait is bounded: a wait that gives up
+// each), 0 MMA issuer (the warp runs the loop, one elected thread issues; items alternate
+// between two TMEM accumulators), 8-19 dequantisers in three sets that take turns by chunk
+// (one weight row per thread, smem -> registers -> TMEM), 4-7 epilogue (TMEM -> registers,
+// scale, SwiGLU, stores; overlaps the next item's MMAs).  Every wait is bounded: a wait that gives up
 // records MOE_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained and TMEM
 // is freed before exit.
 #include <algorithm>
@@ -52,7 +52,14 @@ constexpr int kTraceChunks = 256;
   } while (0)
 static long long *g_trace = nullptr;
 extern "C" void moe_trace_set(void *buf) { g_trace = (long long *)buf; }
+#define MOE_TC_TRACE_R(ev, c) \
+  do {                         \
+    if (r == 0) MOE_TC_TRACE(ev, c); \
+  } while (0)
 #else
+#define MOE_TC_TRACE_R(ev, c) \
+  do {                        \
+  } while (0)
 #define MOE_TC_TRACE(ev, c) \
   do {                      \
   } while (0)
@@ -69,16 +76,17 @@ constexpr int kMaxIssuers = 4;
 constexpr int kMaxStages = 16;
 constexpr int kMaxRuns = 24;
 
-// MMA issuer threads take turns by chunk, each accumulating into its own TMEM accumulator
-// (NMAX columns, NMAX = the launch's largest B row count); the epilogue sums them.  A
-// thread waits ~100-150 cycles per tcgen05 instruction it issues, so two issuers keep the
-// tensor pipe fed (every item has at least two chunks, so both always contribute).  TMEM
-// (512 columns) holds the accumulators and up to 15 chunk stages of dequantised codes (32
-// columns each).  Shared memory holds the code-run ring and the activation-tile ring.
+// One MMA issuer warp (issuing from converged code costs about one MMA's math time at
+// N = 128).  The accumulator (NMAX columns, NMAX = the launch's largest B row count) is
+// double-buffered by item parity, so that the epilogue of one item overlaps the MMAs of
+// the next.  TMEM (512 columns) holds the two accumulators and up to 15 chunk stages of
+// dequantised codes (32 columns each).  Shared memory holds the code-run ring and the
+// activation-tile ring.
 template <int NMAX>
 struct Plan {
-  static constexpr int issuers = 2;
-  static constexpr int stages_fit = (512 - issuers * NMAX) / 32;
+  static constexpr int issuers = 1;
+  static constexpr int acc_bufs = 2;
+  static constexpr int stages_fit = (512 - acc_bufs * NMAX) / 32;
   static constexpr int stages = stages_fit < kMaxStages ? stages_fit : kMaxStages;
   static constexpr int acc_col = stages * 32;
   static constexpr int a_ring = NMAX <= 32 ? 96 * 1024 : 64 * 1024;
@@ -90,10 +98,11 @@ struct TcBars {
   uint64_t b_full[kMaxRuns], b_empty[kMaxRuns];  // activation-tile runs (smem)
   uint64_t t_full[kMaxStages];                   // codes dequantised into a TMEM stage
   uint64_t done[kMaxStages];                     // the chunk's MMAs completed
-  uint64_t acc_full, acc_empty;
+  uint64_t acc_full[2], acc_empty[2];  // per accumulator buffer
   uint64_t drain[kMaxIssuers];
   uint32_t tmem_base;
   int abort_flag;
+  float escale[4][kTcMaxRows];  // gate/up epilogue, per warp: the item's per-row act. scales
 };
 
 template <int NMAX>
@@ -129,6 +138,24 @@ __device__ __forceinline__ void dequant_row(const uint8_t *src, int lane, uint32
   }
 }
 
+// Position in a ring of S stages (stage, phase parity), advanced one step at a time: the
+// ring sizes and run lengths are launch parameters, and stepping avoids integer division.
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int S) {
+    if (++s == S) { s = 0; ph ^= 1; }
+  }
+};
+// A chunk's place in runs of R chunks that occupy a ring of S stages.
+struct RunPos {
+  int j = 0;  // chunk within its run
+  Ring r;     // the run's stage
+  __device__ __forceinline__ void next(int R, int S) {
+    if (++j == R) { j = 0; r.next(S); }
+  }
+};
+
 template <int BITS, bool DOWN, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int item_bound) {
   using PL = Plan<NMAX>;
@@ -150,18 +177,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; s++) {
       tc::mbar_init(&bars->a_full[s], 1);
-      tc::mbar_init(&bars->a_empty[s], 128 * ra);  // every dequantiser thread of every chunk
+      tc::mbar_init(&bars->a_empty[s], 4 * ra);  // every dequantiser warp of every chunk
     }
     for (int s = 0; s < SB; s++) {
       tc::mbar_init(&bars->b_full[s], 1);
       tc::mbar_init(&bars->b_empty[s], rb < NI ? rb : NI);  // issuers with a chunk in the run
     }
     for (int s = 0; s < ST; s++) {
-      tc::mbar_init(&bars->t_full[s], 128);
+      tc::mbar_init(&bars->t_full[s], 4);  // the set's 4 warps
       tc::mbar_init(&bars->done[s], 1);
     }
-    tc::mbar_init(&bars->acc_full, NI);
-    tc::mbar_init(&bars->acc_empty, 128);
+    for (int b = 0; b < 2; b++) {
+      tc::mbar_init(&bars->acc_full[b], NI);
+      tc::mbar_init(&bars->acc_empty[b], 4);  // the 4 epilogue warps
+    }
     for (int i = 0; i < NI; i++) tc::mbar_init(&bars->drain[i], 1);
     bars->abort_flag = 0;
     tc::fence_barrier_init();
@@ -186,14 +215,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       uint64_t *empty = isA ? bars->a_empty : bars->b_empty;
       uint32_t armed = 0, last_ph = 0;
       int run = 0;
+      Ring pos;
       bool ok = true;
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
         if (!tc_item<DOWN>(a, item, it)) break;
-        for (int kc = 0; kc < it.KC; kc += R, run++) {
-          const int s = run % S;
-          const uint32_t ph = (run / S) & 1;
-          if (!tc::mbar_wait(&empty[s], ph ^ 1, abort, lim)) { ok = false; break; }
+        // the item's activation tiles are one contiguous range, read again by the group's
+        // other m-tiles: start it towards L2 now, so that the ring's copies hit L2
+        if (!isA) tc::bulk_prefetch_l2(b_src<DOWN>(a, it, 0), (uint32_t)it.KC * it.rows8 * 128);
+        for (int kc = 0; kc < it.KC; kc += R, run++, pos.next(S)) {
+          const int s = pos.s;
+          const uint32_t ph = pos.ph;
+          if (!tc::mbar_wait_backoff(&empty[s], ph ^ 1, abort, lim, 64)) { ok = false; break; }
           if (isA) {
             tc::mbar_arrive_expect_tx(&full[s], (uint32_t)a_run);
             tc::bulk_g2s(aring + s * a_run, a_src<BITS, DOWN>(a, it, kc), a_run, &full[s]);
@@ -217,43 +250,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     }
   } else if (warp < 4) {
     // ------------------------------------------------ MMA issuers: chunk c goes to c % NI
-    if (lane == 0 && warp < NI) {
+    // The whole warp runs the loop (uniform control flow and operands); one elected lane
+    // issues the tcgen05 instructions.
+    if (warp < NI) {
       const int me = warp;
+      const bool leader = tc::elect_one();
       int c = 0, n = 0;
+      Ring tpos;    // TMEM stage of chunk c
+      RunPos bpos;  // activation-tile run of chunk c
       bool ok = true, issued = false;
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
         if (!tc_item<DOWN>(a, item, it)) break;
-        if (!tc::mbar_wait(&bars->acc_empty, (n & 1) ^ 1, abort, lim)) { ok = false; break; }
+        // accumulator buffer n & 1, used for the (n >> 1)-th time
+        ok = __all_sync(0xffffffffu,
+                        tc::mbar_wait(&bars->acc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort, lim));
+        if (!ok) break;
         tc::fence_after_sync();
         const uint32_t idesc = tc::idesc_f16(0, it.Npad);  // fp16 x fp16 -> fp32
-        const uint32_t dcol = tbase + PL::acc_col + me * NMAX;
+        const uint32_t dcol = tbase + PL::acc_col + ((n & 1) * NI + me) * NMAX;
         bool first = true;
-        for (int kc = 0; kc < it.KC; kc++, c++) {
+        for (int kc = 0; kc < it.KC; kc++, c++, tpos.next(ST), bpos.next(rb, SB)) {
           if (c % NI != me) continue;
-          const int st = c % ST, brun = c / rb, sb = brun % SB;
-          const uint32_t pt = (c / ST) & 1, pb = (brun / SB) & 1;
-          if (!tc::mbar_wait(&bars->t_full[st], pt, abort, lim) ||
-              !tc::mbar_wait(&bars->b_full[sb], pb, abort, lim)) { ok = false; break; }
+          const int st = tpos.s, sb = bpos.r.s;
+          const uint32_t pt = tpos.ph, pb = bpos.r.ph;
+          ok = __all_sync(0xffffffffu, tc::mbar_wait_spin(&bars->t_full[st], pt, abort, lim) &&
+                                           tc::mbar_wait_spin(&bars->b_full[sb], pb, abort, lim));
+          if (!ok) break;
           tc::fence_after_sync();
-          MOE_TC_TRACE(5, c);
-          const uint32_t bsm = tc::smem_u32(bring + sb * b_stride) + (c % rb) * it.rows8 * 128;
+          if (leader) MOE_TC_TRACE(5, c);
+          const uint32_t bsm = tc::smem_u32(bring + sb * b_stride) + bpos.j * it.rows8 * 128;
+          const bool last_of_run = bpos.j + NI >= rb || kc + NI >= it.KC;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++)
-            tc::mma_ts(dcol, tbase + st * 32 + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
-                       !(first && kk == 0));
+            for (int kk = 0; kk < 4; kk++)
+              tc::mma_ts(dcol, tbase + st * 32 + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
+                         !(first && kk == 0));
+            MOE_TC_TRACE(3, c);
+            tc::mma_commit(&bars->done[st]);
+            if (last_of_run) tc::mma_commit(&bars->b_empty[sb]);  // my last chunk of the run
+            MOE_TC_TRACE(6, c);
+          }
+          __syncwarp();
           first = false;
           issued = true;
-          MOE_TC_TRACE(3, c);
-          tc::mma_commit(&bars->done[st]);
-          if ((c + NI) / rb != brun || kc + NI >= it.KC)  // my last chunk of the run
-            tc::mma_commit(&bars->b_empty[sb]);
-          MOE_TC_TRACE(6, c);
         }
         if (!ok) break;
-        tc::mma_commit(&bars->acc_full);
+        if (leader) tc::mma_commit(&bars->acc_full[n & 1]);
+        __syncwarp();
       }
-      if (!ok) {
+      if (!ok && leader) {
         give_up();
         if (issued) {  // all MMAs issued so far complete before TMEM is freed
           tc::mma_commit(&bars->drain[me]);
@@ -265,29 +311,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     // ------------------------------------------------ dequantisers: one weight row a thread
     const int q = warp & 3, r = 32 * q + lane, set = (warp - kDqWarp0) >> 2;
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
-    int c = 0;  // running chunk index over all items of this CTA (all roles count alike)
+    int c = 0;     // running chunk index over all items of this CTA (all roles count alike)
+    int turn = 0;  // c % kDqSets: the set that takes chunk c
+    Ring tpos;     // TMEM stage of chunk c
+    RunPos apos;   // code run of chunk c
     bool ok = true;
     Item it;
     for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
       if (!tc_item<DOWN>(a, item, it)) break;
-      for (int kc = 0; kc < it.KC; kc++, c++) {
-        if (c % kDqSets != set) continue;
-        const int arun = c / ra, sa = arun % SA, st = c % ST;
-        const uint32_t pa = (arun / SA) & 1, pt = (c / ST) & 1;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->a_full[sa], pa, abort, lim));
+      for (int kc = 0; kc < it.KC; kc++, c++, turn = turn + 1 == kDqSets ? 0 : turn + 1,
+               tpos.next(ST), apos.next(ra, SA)) {
+        if (turn != set) continue;
+        const int sa = apos.r.s, st = tpos.s;
+        const uint32_t pa = apos.r.ph, pt = tpos.ph;
+        ok = __all_sync(0xffffffffu, tc::mbar_wait_backoff(&bars->a_full[sa], pa, abort, lim, 32));
         if (!ok) break;
-        if (r == 0) MOE_TC_TRACE(2, c);
+        MOE_TC_TRACE_R(2, c);
         uint32_t v[32];
-        dequant_row<BITS>(aring + sa * a_run + (c % ra) * AB + r * RB, lane, v);
-        tc::mbar_arrive(&bars->a_empty[sa]);
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[st], pt ^ 1, abort, lim));
+        dequant_row<BITS>(aring + sa * a_run + apos.j * AB + r * RB, lane, v);
+        __syncwarp();  // the warp's shared-memory reads are done: one arrival per warp
+        if (lane == 0) tc::mbar_arrive(&bars->a_empty[sa]);
+        ok = __all_sync(0xffffffffu, tc::mbar_wait_backoff(&bars->done[st], pt ^ 1, abort, lim, 32));
         if (!ok) break;
+        MOE_TC_TRACE_R(7, c);
         tc::fence_after_sync();
         tc::tmem_st32(tbase + tlane + st * 32, v);
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        tc::mbar_arrive(&bars->t_full[st]);
-        if (r == 0) MOE_TC_TRACE(4, c);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bars->t_full[st]);
+        MOE_TC_TRACE_R(4, c);
       }
     }
     if (!ok && lane == 0) give_up();
@@ -295,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     // ------------------------------------------------ epilogue: one output row a thread
     const int q = warp & 3, r = 32 * q + lane;
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
-    const uint32_t d0 = tbase + tlane + PL::acc_col;
+    uint32_t d0 = tbase + tlane + PL::acc_col;  // + the item's buffer
     // sum of the issuers' accumulators, 16 columns from c0
     auto load_sum = [&](int c0, float (&v)[16]) {
 #pragma unroll
@@ -312,14 +365,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     Item it;
     for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
       if (!tc_item<DOWN>(a, item, it)) break;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->acc_full, n & 1, abort, lim));
+      ok = __all_sync(0xffffffffu,
+                      tc::mbar_wait_backoff(&bars->acc_full[n & 1], (n >> 1) & 1, abort, lim, 256));
+      d0 = tbase + tlane + PL::acc_col + (n & 1) * NI * NMAX;
       if (!ok) break;
+      MOE_TC_TRACE_R(8, n);
       tc::fence_after_sync();
       const ExpertLayout &L = it.sh ? a.LS : a.LR;
       const int gn = it.g.n;
       if (!DOWN) {
         const float s = ((const float *)(it.ebase + L.sgu_off))[it.mt * 128 + r];
-        const float *rsc = a.rscale + it.g.xrow0;  // 1 / the token's activation scale
+        // 1 / the token's activation scale, per B row: loaded once per item into this warp's
+        // slice of shared memory (no load waits behind the stores of the loop below)
+        float *rsc = bars->escale[q];
+        __syncwarp();
+        for (int i = lane; i < it.Npad; i += 32)
+          rsc[i] = i < it.rowsB ? a.rscale[it.g.xrow0 + i] : 0.f;
+        __syncwarp();
         const int j = r >> 1;  // output index within the m-tile (64 outputs)
         uint8_t *hbase =
             a.hg + (size_t)it.g.hrow0 * a.Imax * 2 + (size_t)it.mt * round8(gn) * 128;
@@ -332,9 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
             if (a.P == 2 && (jj & 1)) continue;  // the lo piece, folded into its hi column
             float v = acc[jj];
             if (a.P == 2) v += acc[(jj + 1) & 15];
-            v *= s * (c0 + jj < it.rowsB ? rsc[c0 + jj] : 0.f);
+            v *= s * rsc[c0 + jj];
             const float up = __shfl_xor_sync(0xffffffffu, v, 1);
-            const int i = (c0 + jj) / a.P;  // token within the group
+            const int i = a.P == 2 ? (c0 + jj) >> 1 : c0 + jj;  // token within the group
             if ((r & 1) == 0 && i < gn) {
               const __half hv = __float2half_rn(silu_f(v) * up);
               bad |= __hisinf(hv) || __hisnan(hv);
@@ -356,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         }
       }
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->acc_empty);
+      __syncwarp();
+      MOE_TC_TRACE_R(9, n);
+      if (lane == 0) tc::mbar_arrive(&bars->acc_empty[n & 1]);
     }
     if (!ok && lane == 0) give_up();
   }

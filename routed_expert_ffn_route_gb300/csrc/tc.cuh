@@ -86,6 +86,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// As mbar_wait, for the critical path: polls without the suspend hint (a suspended thread
+// can take on the order of a microsecond to resume after the phase completes), checking
+// the abort flag and the time limit every 64 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity,
+                                               volatile int *abort, long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; i++)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((long)(global_ns() - t0) > limit_ns) return false;
+  }
+}
+
+// As mbar_wait, but a thread that has to wait sleeps `sleep_ns` between polls, so that
+// warps whose wait is not on the critical path leave the barrier unit and the issue slots
+// to those whose wait is.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort, long limit_ns,
+                                                  uint32_t sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if ((long)(global_ns() - t0) > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------- bulk copy (TMA, 1-D)
 // global -> shared, completion counted in bytes on `bar`.  dst, src 16-byte aligned,
 // bytes a multiple of 16.
@@ -96,6 +127,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
           "r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Start loading [src, src + bytes) into L2 (no completion to wait for).  src 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------- cp.async (16 B per thread)
@@ -206,6 +243,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   d |= (uint64_t)1 << 46;                  // fixed 0b001
   d |= (uint64_t)2 << 61;                  // swizzle 128B
   return d;
+}
+
+// One lane of a converged warp (the same lane on every call).  Code that the whole warp
+// runs keeps warp-uniform values in uniform registers, which tcgen05 instructions take
+// directly; only the instruction itself is issued by the elected lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, A/B type (0 = f16, 1 = bf16),
