@@ -4,7 +4,8 @@
 // MoE引擎", §3.2 Step 1 gate projection; "colibrì 深度拆解", §4.3 router_forward).
 //  - T <= 16: a GEMV split over (8 experts) x (H/8 slices) per CTA so that all SMs stream the
 //    fp32 router matrix at once; the 8 partial sums are added in a fixed order afterwards.
-//  - T > 16: a tiled CUDA-core GEMM (64 tokens x 64 experts per CTA).
+//  - T > 16: a tiled CUDA-core GEMM (128 x 128 or 64 x 64 tiles, 8 x 8 or 4 x 4 outputs a
+//    thread), the H dimension split across CTAs as for the GEMV.
 // Selection, one warp per token:
 //  - softmax router: softmax with the maximum subtracted, the k largest, renormalised
 //    (§3.2 Steps 2-3 of the same page);
@@ -76,52 +77,124 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(moe_layer_config c, co
   }
 }
 
-// Tiled fp32 GEMM: partials[0][t][e] = sum_h x[t][h] Wr[e][h]; 64x64 tile, 4x4 per thread.
-__global__ void __launch_bounds__(256) router_gemm_kernel(moe_layer_config c, const uint8_t *packed,
-                                                          const float *wr, const void *x,
-                                                          int is_bf16, int T, float *partials,
-                                                          Ctrl *ctrl) {
-  __shared__ float As[32][64 + 4];  // [k][token]
-  __shared__ float Bs[32][64 + 4];  // [k][expert]
+// Tiled fp32 GEMM over one H slice: partials[hs][t][e] = sum over h in slice hs of
+// x[t][h] * Wr[e][h].  A CTA computes BM tokens x BN experts in k-steps of 8; each thread
+// a TM x TN block from float4 shared-memory reads (tokens and experts stored k-major in
+// shared memory).  The next k-step's tiles are loaded into registers while the current
+// one is multiplied, and shared memory is double-buffered, so one barrier per k-step.
+template <int BM, int BN, int TM, int TN>
+__global__ void __launch_bounds__((BM / TM) * (BN / TN))
+    router_gemm_kernel(moe_layer_config c, const uint8_t *packed, const float *wr, const void *x,
+                       int is_bf16, int T, int hslice, float *partials, Ctrl *ctrl) {
+  constexpr int NT = (BM / TM) * (BN / TN), BK = 8;
+  constexpr int LA = BM * BK / NT, LB = BN * BK / NT;  // elements a thread loads per k-step
+  static_assert(LA == 2 || LA == 4, "A loads of 2 or 4 elements");
+  static_assert(LB == 2 || LB == 4, "B loads of 2 or 4 elements");
+  __shared__ __align__(16) float As[2][BK][BM];
+  __shared__ __align__(16) float Bs[2][BK][BN];
   const int H = c.hidden, E = c.n_experts;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_header(packed, c, ctrl);
-  const int t0 = blockIdx.y * 64, e0 = blockIdx.x * 64;
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < H; k0 += 32) {
-    for (int i = threadIdx.x; i < 64 * 32; i += 256) {
-      int r = i / 32, kk = i % 32;
-      int t = t0 + r, e = e0 + r;
-      float xv = 0.f, wv = 0.f;
-      if (t < T) {
-        long src = (long)t * H + k0 + kk;
-        xv = is_bf16 ? bf16_to_f32(((const uint16_t *)x)[src]) : ((const float *)x)[src];
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+    check_header(packed, c, ctrl);
+  const int t0 = blockIdx.y * BM, e0 = blockIdx.x * BN, hs = blockIdx.z;
+  const int tid = threadIdx.x;
+  // loader mapping: row, first k of the thread's LA (LB) consecutive elements
+  const int am = tid / (BK / LA), ak = (tid % (BK / LA)) * LA;
+  const int bn = tid / (BK / LB), bk = (tid % (BK / LB)) * LB;
+  const int ta = t0 + am, eb = e0 + bn;
+  const long xrow = (long)(ta < T ? ta : 0) * H + (long)hs * hslice + ak;
+  const long wrow = (long)(eb < E ? eb : 0) * H + (long)hs * hslice + bk;
+  float ra[LA], rb[LB];
+  auto load = [&](int k0) {
+    if (ta < T) {
+      if (is_bf16) {
+        const uint16_t *p = (const uint16_t *)x + xrow + k0;
+        if (LA == 4) {
+          const uint2 u = *(const uint2 *)p;
+          ra[0] = __uint_as_float(u.x << 16);
+          ra[1] = __uint_as_float(u.x & 0xFFFF0000u);
+          ra[LA > 2 ? 2 : 0] = __uint_as_float(u.y << 16);
+          ra[LA > 2 ? 3 : 1] = __uint_as_float(u.y & 0xFFFF0000u);
+        } else {
+          const uint32_t u = *(const uint32_t *)p;
+          ra[0] = __uint_as_float(u << 16);
+          ra[1] = __uint_as_float(u & 0xFFFF0000u);
+        }
+      } else {
+        const float *p = (const float *)x + xrow + k0;
+        if (LA == 4) {
+          const float4 f = *(const float4 *)p;
+          ra[0] = f.x; ra[1] = f.y; ra[LA > 2 ? 2 : 0] = f.z; ra[LA > 2 ? 3 : 1] = f.w;
+        } else {
+          const float2 f = *(const float2 *)p;
+          ra[0] = f.x; ra[1] = f.y;
+        }
       }
-      if (e < E) wv = __ldg(wr + (long)e * H + k0 + kk);
-      As[kk][r] = xv;
-      Bs[kk][r] = wv;
+    } else {
+#pragma unroll
+      for (int i = 0; i < LA; i++) ra[i] = 0.f;
     }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < 32; kk++) {
-      float a[4], b[4];
+    if (eb < E) {
+      const float *p = wr + wrow + k0;
+      if (LB == 4) {
+        const float4 f = __ldg((const float4 *)p);
+        rb[0] = f.x; rb[1] = f.y; rb[LB > 2 ? 2 : 0] = f.z; rb[LB > 2 ? 3 : 1] = f.w;
+      } else {
+        const float2 f = __ldg((const float2 *)p);
+        rb[0] = f.x; rb[1] = f.y;
+      }
+    } else {
 #pragma unroll
-      for (int i = 0; i < 4; i++) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; }
-#pragma unroll
-      for (int i = 0; i < 4; i++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      for (int i = 0; i < LB; i++) rb[i] = 0.f;
     }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < LA; i++) As[buf][ak + i][am] = ra[i];
+#pragma unroll
+    for (int i = 0; i < LB; i++) Bs[buf][bk + i][bn] = rb[i];
+  };
+  const int tx = tid % (BN / TN), ty = tid / (BN / TN);
+  float acc[TM][TN];
+#pragma unroll
+  for (int i = 0; i < TM; i++)
+#pragma unroll
+    for (int j = 0; j < TN; j++) acc[i][j] = 0.f;
+  const int nks = hslice / BK;
+  load(0);
+  store(0);
+  __syncthreads();
+  for (int ks = 0; ks < nks; ks++) {
+    const int buf = ks & 1;
+    if (ks + 1 < nks) load((ks + 1) * BK);
+#pragma unroll
+    for (int k = 0; k < BK; k++) {
+      float a[TM], b[TN];
+#pragma unroll
+      for (int i = 0; i < TM; i += 4) {
+        const float4 v = *(const float4 *)&As[buf][k][ty * TM + i];
+        a[i] = v.x; a[i + 1] = v.y; a[i + 2] = v.z; a[i + 3] = v.w;
+      }
+#pragma unroll
+      for (int j = 0; j < TN; j += 4) {
+        const float4 v = *(const float4 *)&Bs[buf][k][tx * TN + j];
+        b[j] = v.x; b[j + 1] = v.y; b[j + 2] = v.z; b[j + 3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; i++)
+#pragma unroll
+        for (int j = 0; j < TN; j++) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (ks + 1 < nks) store(buf ^ 1);
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; i++) {
-    int t = t0 + ty * 4 + i;
+  for (int i = 0; i < TM; i++) {
+    const int t = t0 + ty * TM + i;
     if (t >= T) continue;
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      int e = e0 + tx * 4 + j;
-      if (e < E) partials[(long)t * E + e] = acc[i][j];
+    for (int j = 0; j < TN; j++) {
+      const int e = e0 + tx * TN + j;
+      if (e < E) partials[((long)hs * T + t) * E + e] = acc[i][j];
     }
   }
 }
@@ -327,9 +400,22 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
     else GEMV(16);
 #undef GEMV
   } else {
+    // 128 x 128 tiles for large T, 64 x 64 below; H split (partial sums added in order by
+    // the selection kernel) until the grid covers the SMs twice
+    const bool big = T >= 256;
+    const int BM = big ? 128 : 64, BN = big ? 128 : 64;
+    const int tiles = ((T + BM - 1) / BM) * ((c.n_experts + BN - 1) / BN);
+    const int sms = dev_info().sms;
     hsplits = 1;
-    dim3 grid((c.n_experts + 63) / 64, (T + 63) / 64);
-    router_gemm_kernel<<<grid, 256, 0, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl);
+    while (hsplits < kRouterHS && tiles * hsplits < 2 * sms) hsplits *= 2;
+    const int hslice = c.hidden / hsplits;  // a multiple of 16: hidden % 128 == 0
+    dim3 grid((c.n_experts + BN - 1) / BN, (T + BM - 1) / BM, hsplits);
+    if (big)
+      router_gemm_kernel<128, 128, 8, 8><<<grid, 256, 0, st>>>(c, packed, wr, x, is_bf16, T, hslice,
+                                                               partials, ctrl);
+    else
+      router_gemm_kernel<64, 64, 4, 4><<<grid, 256, 0, st>>>(c, packed, wr, x, is_bf16, T, hslice,
+                                                             partials, ctrl);
   }
   const float *bias = (const float *)(packed + P.router_b_off);
   float *tscale = W.tc ? (float *)(ws + W.tscale) : nullptr;
