@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
               const float up = __shfl_xor_sync(0xffffffffu, v[hh][q], 4);  // row r + 1: lane + 4
               const int i = tok[q], jo = (hh ? r1 : r0) >> 1;  // token; output within the m-tile
               if ((g & 1) == 0 && i < gn) {
-                const __half hv = __float2half_rn(silu_f(v[hh][q]) * up);
+                const __half hv = __float2half_rn(silu_fast(v[hh][q]) * up);
                 bad |= __hisinf(hv) || __hisnan(hv);
                 *(__half *)(hbase + (size_t)i * 128 + (((jo >> 3) ^ (i & 7)) << 4) + (jo & 7) * 2) =
                     hv;

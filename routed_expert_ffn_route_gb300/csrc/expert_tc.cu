@@ -73,6 +73,10 @@ constexpr int kProdWarp0 = kDqWarp0 + 4 * kDqSets;
 constexpr int kWarps = kProdWarp0 + 2;
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxIssuers = 4;
+// Chunks per hand-off between the dequantisers and the MMA issuer (one TMEM stage): a
+// barrier round trip costs a few hundred cycles on a busy SM, so each one covers 8 MMAs.
+// Every K is a multiple of 128, so every item has a whole number of units.
+constexpr int kUnit = 2;
 constexpr int kMaxStages = 16;
 constexpr int kMaxRuns = 24;
 
@@ -86,11 +90,19 @@ template <int NMAX>
 struct Plan {
   static constexpr int issuers = 1;
   static constexpr int acc_bufs = 2;
-  static constexpr int stages_fit = (512 - acc_bufs * NMAX) / 32;
+  static constexpr int stage_cols = 32 * kUnit;
+  static constexpr int stages_fit = (512 - acc_bufs * NMAX) / stage_cols;
   static constexpr int stages = stages_fit < kMaxStages ? stages_fit : kMaxStages;
-  static constexpr int acc_col = stages * 32;
-  static constexpr int a_ring = NMAX <= 32 ? 96 * 1024 : 64 * 1024;
-  static constexpr int b_ring = NMAX <= 32 ? 112 * 1024 : 128 * 1024;
+  static constexpr int acc_col = stages * stage_cols;
+};
+
+// Shared-memory rings.  Each code run (16 KB at int4) covers several chunks, so three runs
+// (two at int8) give ample lookahead; everything else goes to the activation-tile ring,
+// whose copies wait on the most latency (tiles read by many CTAs, across both dies' L2).
+template <int NMAX, int BITS>
+struct Rings {
+  static constexpr int a_ring = BITS == 8 ? 64 * 1024 : 48 * 1024;
+  static constexpr int b_ring = 220 * 1024 - a_ring;
 };
 
 struct TcBars {
@@ -105,9 +117,9 @@ struct TcBars {
   float escale[4][kTcMaxRows];  // gate/up epilogue, per warp: the item's per-row act. scales
 };
 
-template <int NMAX>
+template <int NMAX, int BITS>
 constexpr size_t tc_smem() {
-  return 1024 + (size_t)Plan<NMAX>::a_ring + Plan<NMAX>::b_ring + sizeof(TcBars);
+  return 1024 + (size_t)Rings<NMAX, BITS>::a_ring + Rings<NMAX, BITS>::b_ring + sizeof(TcBars);
 }
 
 // One weight row's 64 codes (one k-chunk) -> 32 pairs of exact fp16 integers (element 2c
@@ -156,23 +168,28 @@ struct RunPos {
   }
 };
 
-template <int BITS, bool DOWN, int NMAX>
+// CL = 2: CTAs run in clusters of two that take adjacent m-tiles of the same group (items
+// 2p and 2p + 1), so that they read the same activation tiles: each run of tiles is loaded
+// once, by the two CTAs in turn, and multicast into both; a ring stage is refilled once
+// both CTAs' MMAs have released it.
+template <int BITS, bool DOWN, int NMAX, int CL>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int item_bound) {
   using PL = Plan<NMAX>;
+  using RG = Rings<NMAX, BITS>;
   constexpr int ST = PL::stages, NI = PL::issuers;
   constexpr int AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
   extern __shared__ uint8_t smraw[];
   uint8_t *base = tc::align_smem_1024(smraw);
   uint8_t *bring = base;
-  uint8_t *aring = base + PL::b_ring;
-  TcBars *bars = (TcBars *)(aring + PL::a_ring);
+  uint8_t *aring = base + RG::b_ring;
+  TcBars *bars = (TcBars *)(aring + RG::a_ring);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int where = DOWN ? kKDown : kKGateUp;
   // ring geometry of this launch
   const int ra = a.ra, rb = a.rb;
   const int a_run = ra * AB;                                  // bytes of a code run
   const int b_stride = (rb + (rb > 1 ? 1 : 0)) * NMAX * 128;  // run + the MMA's over-read
-  const int SA = min(kMaxRuns, PL::a_ring / a_run), SB = min(kMaxRuns, PL::b_ring / b_stride);
+  const int SA = min(kMaxRuns, RG::a_ring / a_run), SB = min(kMaxRuns, RG::b_ring / b_stride);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; s++) {
@@ -181,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     }
     for (int s = 0; s < SB; s++) {
       tc::mbar_init(&bars->b_full[s], 1);
-      tc::mbar_init(&bars->b_empty[s], rb < NI ? rb : NI);  // issuers with a chunk in the run
+      tc::mbar_init(&bars->b_empty[s], CL * (rb < NI ? rb : NI));  // each CTA's issuers
     }
     for (int s = 0; s < ST; s++) {
       tc::mbar_init(&bars->t_full[s], 4);  // the set's 4 warps
@@ -198,7 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   if (warp == 0) tc::tmem_alloc<512>(&bars->tmem_base);
   tc::fence_before_sync();
   __syncthreads();
+  if (CL == 2) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::fence_after_sync();
+  const uint32_t crank = CL == 2 ? tc::cluster_rank() : 0;
   const uint32_t tbase = bars->tmem_base;
   volatile int *abort = &bars->abort_flag;
   const long lim = a.wait_limit;
@@ -222,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         if (!tc_item<DOWN>(a, item, it)) break;
         // the item's activation tiles are one contiguous range, read again by the group's
         // other m-tiles: start it towards L2 now, so that the ring's copies hit L2
-        if (!isA) tc::bulk_prefetch_l2(b_src<DOWN>(a, it, 0), (uint32_t)it.KC * it.rows8 * 128);
+        if (!isA && CL == 1)
+          tc::bulk_prefetch_l2(b_src<DOWN>(a, it, 0), (uint32_t)it.KC * it.rows8 * 128);
         for (int kc = 0; kc < it.KC; kc += R, run++, pos.next(S)) {
           const int s = pos.s;
           const uint32_t ph = pos.ph;
@@ -233,8 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
             MOE_TC_TRACE(0, run * R);
           } else {
             const uint32_t bytes = (uint32_t)R * it.rows8 * 128;
-            tc::mbar_arrive_expect_tx(&full[s], bytes);
-            tc::bulk_g2s(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes, &full[s]);
+            tc::mbar_arrive_expect_tx(&full[s], bytes);  // every run lands here
+            if (CL == 1)
+              tc::bulk_g2s(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes, &full[s]);
+            else if ((uint32_t)(run & 1) == crank)  // runs alternate between the two CTAs
+              tc::bulk_g2s_multicast(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes,
+                                     &full[s], 0x3);
             MOE_TC_TRACE(1, run * R);
           }
           armed |= 1u << s;
@@ -249,50 +273,60 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       }
     }
   } else if (warp < 4) {
-    // ------------------------------------------------ MMA issuers: chunk c goes to c % NI
+    // ------------------------------------------------ MMA issuer
     // The whole warp runs the loop (uniform control flow and operands); one elected lane
-    // issues the tcgen05 instructions.
-    if (warp < NI) {
-      const int me = warp;
+    // waits and issues the tcgen05 instructions.  A unit of kUnit chunks needs one wait: its
+    // dequantiser set publishes the TMEM stage only once the chunks' activation tiles landed.
+    static_assert(NI == 1, "one issuer");
+    if (warp == 0) {
       const bool leader = tc::elect_one();
       int c = 0, n = 0;
-      Ring tpos;    // TMEM stage of chunk c
+      Ring tpos;    // TMEM stage of the unit
       RunPos bpos;  // activation-tile run of chunk c
       bool ok = true, issued = false;
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
         if (!tc_item<DOWN>(a, item, it)) break;
         // accumulator buffer n & 1, used for the (n >> 1)-th time
-        ok = __all_sync(0xffffffffu,
-                        tc::mbar_wait(&bars->acc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort, lim));
+        int got = 1;
+        if (leader) got = tc::mbar_wait(&bars->acc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort, lim);
+        ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t idesc = tc::idesc_f16(0, it.Npad);  // fp16 x fp16 -> fp32
-        const uint32_t dcol = tbase + PL::acc_col + ((n & 1) * NI + me) * NMAX;
-        bool first = true;
-        for (int kc = 0; kc < it.KC; kc++, c++, tpos.next(ST), bpos.next(rb, SB)) {
-          if (c % NI != me) continue;
-          const int st = tpos.s, sb = bpos.r.s;
-          const uint32_t pt = tpos.ph, pb = bpos.r.ph;
-          ok = __all_sync(0xffffffffu, tc::mbar_wait_spin(&bars->t_full[st], pt, abort, lim) &&
-                                           tc::mbar_wait_spin(&bars->b_full[sb], pb, abort, lim));
+        const uint32_t dcol = tbase + PL::acc_col + (n & 1) * NMAX;
+        for (int ku = 0; ku < it.KC; ku += kUnit, tpos.next(ST)) {
+          got = 1;
+          if (leader) MOE_TC_TRACE(10, c);
+          if (leader) got = tc::mbar_wait_spin(&bars->t_full[tpos.s], tpos.ph, abort, lim);
+          if (leader) MOE_TC_TRACE(11, c);
+          ok = __all_sync(0xffffffffu, got);
           if (!ok) break;
           tc::fence_after_sync();
           if (leader) MOE_TC_TRACE(5, c);
-          const uint32_t bsm = tc::smem_u32(bring + sb * b_stride) + bpos.j * it.rows8 * 128;
-          const bool last_of_run = bpos.j + NI >= rb || kc + NI >= it.KC;
-          if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < 4; kk++)
-              tc::mma_ts(dcol, tbase + st * 32 + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
-                         !(first && kk == 0));
-            MOE_TC_TRACE(3, c);
-            tc::mma_commit(&bars->done[st]);
-            if (last_of_run) tc::mma_commit(&bars->b_empty[sb]);  // my last chunk of the run
-            MOE_TC_TRACE(6, c);
+          for (int j = 0; j < kUnit; j++, c++, bpos.next(rb, SB)) {
+            const uint32_t bsm =
+                tc::smem_u32(bring + bpos.r.s * b_stride) + bpos.j * it.rows8 * 128;
+            const uint32_t acol = tbase + tpos.s * PL::stage_cols + j * 32;
+            const bool last_of_run = bpos.j + 1 >= rb || ku + j + 1 >= it.KC;
+            if (leader) {
+#pragma unroll
+              for (int kk = 0; kk < 4; kk++)
+                tc::mma_ts(dcol, acol + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
+                           ku + j + kk > 0);
+              if (last_of_run) {  // the run's last chunk: release the stage (in both CTAs)
+                if (CL == 1) tc::mma_commit(&bars->b_empty[bpos.r.s]);
+                else tc::mma_commit_multicast(&bars->b_empty[bpos.r.s], 0x3);
+              }
+            }
+          }
+          if (leader) {
+            MOE_TC_TRACE(3, c - 1);
+            tc::mma_commit(&bars->done[tpos.s]);
+            MOE_TC_TRACE(6, c - 1);
           }
           __syncwarp();
-          first = false;
           issued = true;
         }
         if (!ok) break;
@@ -302,45 +336,65 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       if (!ok && leader) {
         give_up();
         if (issued) {  // all MMAs issued so far complete before TMEM is freed
-          tc::mma_commit(&bars->drain[me]);
-          wait_nofail(&bars->drain[me], 0, lim);
+          tc::mma_commit(&bars->drain[0]);
+          wait_nofail(&bars->drain[0], 0, lim);
         }
       }
     }
   } else if (warp >= kDqWarp0) {
     // ------------------------------------------------ dequantisers: one weight row a thread
+    // The sets take units of kUnit chunks in turn; a unit's chunks go to one TMEM stage.
     const int q = warp & 3, r = 32 * q + lane, set = (warp - kDqWarp0) >> 2;
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
     int c = 0;     // running chunk index over all items of this CTA (all roles count alike)
-    int turn = 0;  // c % kDqSets: the set that takes chunk c
-    Ring tpos;     // TMEM stage of chunk c
+    int turn = 0;  // the set that takes the current unit
+    Ring tpos;     // TMEM stage of the unit
     RunPos apos;   // code run of chunk c
+    RunPos bpos;   // activation-tile run of chunk c
     bool ok = true;
     Item it;
     for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
       if (!tc_item<DOWN>(a, item, it)) break;
-      for (int kc = 0; kc < it.KC; kc++, c++, turn = turn + 1 == kDqSets ? 0 : turn + 1,
-               tpos.next(ST), apos.next(ra, SA)) {
-        if (turn != set) continue;
-        const int sa = apos.r.s, st = tpos.s;
-        const uint32_t pa = apos.r.ph, pt = tpos.ph;
-        ok = __all_sync(0xffffffffu, tc::mbar_wait_backoff(&bars->a_full[sa], pa, abort, lim, 32));
-        if (!ok) break;
-        MOE_TC_TRACE_R(2, c);
-        uint32_t v[32];
-        dequant_row<BITS>(aring + sa * a_run + apos.j * AB + r * RB, lane, v);
-        __syncwarp();  // the warp's shared-memory reads are done: one arrival per warp
-        if (lane == 0) tc::mbar_arrive(&bars->a_empty[sa]);
-        ok = __all_sync(0xffffffffu, tc::mbar_wait_backoff(&bars->done[st], pt ^ 1, abort, lim, 32));
+      for (int ku = 0; ku < it.KC; ku += kUnit, turn = turn + 1 == kDqSets ? 0 : turn + 1,
+               tpos.next(ST)) {
+        if (turn != set) {
+#pragma unroll
+          for (int j = 0; j < kUnit; j++, c++) apos.next(ra, SA), bpos.next(rb, SB);
+          continue;
+        }
+        // the stage's previous unit has been multiplied
+        ok = __all_sync(0xffffffffu,
+                        tc::mbar_wait_backoff(&bars->done[tpos.s], tpos.ph ^ 1, abort, lim, 32));
         if (!ok) break;
         MOE_TC_TRACE_R(7, c);
         tc::fence_after_sync();
-        tc::tmem_st32(tbase + tlane + st * 32, v);
+#pragma unroll 1
+        for (int j = 0; j < kUnit; j++, c++, apos.next(ra, SA), bpos.next(rb, SB)) {
+          ok = __all_sync(0xffffffffu, tc::mbar_wait_backoff(&bars->a_full[apos.r.s], apos.r.ph,
+                                                             abort, lim, 32));
+          if (!ok) break;
+          MOE_TC_TRACE_R(2, c);
+          uint32_t v[32];
+          dequant_row<BITS>(aring + apos.r.s * a_run + apos.j * AB + r * RB, lane, v);
+          __syncwarp();  // the warp's shared-memory reads are done: one arrival per warp
+          if (lane == 0) tc::mbar_arrive(&bars->a_empty[apos.r.s]);
+          tc::tmem_st32(tbase + tlane + tpos.s * PL::stage_cols + j * 32, v);
+          if (q == 0) {
+            // the chunk's activation tile has landed: the published stage then stands for
+            // both MMA operands (the tile's ring stage cannot be reused before this chunk's
+            // MMAs: the ring holds at least as many chunks as TMEM has stages)
+            ok = __all_sync(0xffffffffu, tc::mbar_wait_backoff(&bars->b_full[bpos.r.s],
+                                                               bpos.r.ph, abort, lim, 32));
+            if (!ok) break;
+          }
+        }
+        if (!ok) break;
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bars->t_full[st]);
-        MOE_TC_TRACE_R(4, c);
+        if (lane == 0) tc::mbar_arrive(&bars->t_full[tpos.s]);
+        MOE_TC_TRACE_R(4, c - 1);
+        if (lane == 0) MOE_TC_TRACE(12 + q, c - 1);
       }
     }
     if (!ok && lane == 0) give_up();
@@ -383,25 +437,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
           rsc[i] = i < it.rowsB ? a.rscale[it.g.xrow0 + i] : 0.f;
         __syncwarp();
         const int j = r >> 1;  // output index within the m-tile (64 outputs)
+        const bool odd = r & 1;  // rows 2j (gate) and 2j + 1 (up) sit in adjacent lanes
         uint8_t *hbase =
             a.hg + (size_t)it.g.hrow0 * a.Imax * 2 + (size_t)it.mt * round8(gn) * 128;
         bool bad = false;
+        // tokens in pairs (i, i + 1): the gate lane computes h for token i, the up lane for
+        // token i + 1; one exchange gives each lane the other operand it needs
+        auto pair = [&](int i, float w0, float w1) {
+          const float other = __shfl_xor_sync(0xffffffffu, odd ? w0 : w1, 1);
+          const int tok = odd ? i + 1 : i;
+          const float g = odd ? other : w0, u = odd ? w1 : other;
+          if (tok < gn) {
+            const __half hv = __float2half_rn(silu_fast(g) * u);
+            bad |= __hisinf(hv) || __hisnan(hv);
+            *(__half *)(hbase + (size_t)tok * 128 + (((j >> 3) ^ (tok & 7)) << 4) + (j & 7) * 2) =
+                hv;
+          }
+        };
         for (int c0 = 0; c0 < it.Npad; c0 += 16) {
           float acc[16];
           load_sum(c0, acc);
+          if (a.P == 1) {
 #pragma unroll
-          for (int jj = 0; jj < 16; jj++) {
-            if (a.P == 2 && (jj & 1)) continue;  // the lo piece, folded into its hi column
-            float v = acc[jj];
-            if (a.P == 2) v += acc[(jj + 1) & 15];
-            v *= s * rsc[c0 + jj];
-            const float up = __shfl_xor_sync(0xffffffffu, v, 1);
-            const int i = a.P == 2 ? (c0 + jj) >> 1 : c0 + jj;  // token within the group
-            if ((r & 1) == 0 && i < gn) {
-              const __half hv = __float2half_rn(silu_f(v) * up);
-              bad |= __hisinf(hv) || __hisnan(hv);
-              *(__half *)(hbase + (size_t)i * 128 + (((j >> 3) ^ (i & 7)) << 4) + (j & 7) * 2) = hv;
-            }
+            for (int jj = 0; jj < 16; jj += 2)
+              pair(c0 + jj, acc[jj] * s * rsc[c0 + jj], acc[jj + 1] * s * rsc[c0 + jj + 1]);
+          } else {  // columns 2i, 2i + 1: the hi and lo pieces of token i
+#pragma unroll
+            for (int jj = 0; jj < 16; jj += 4)
+              pair((c0 + jj) >> 1, (acc[jj] + acc[jj + 1]) * s * rsc[c0 + jj],
+                   (acc[jj + 2] + acc[jj + 3]) * s * rsc[c0 + jj + 2]);
           }
         }
         if (bad) record_status(a.ctrl, MOE_ERR_NUMERIC, where);
@@ -428,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc<512>(tbase);
+  if (CL == 2) tc::cluster_sync();  // no copy or arrival from the peer is still due here
 }
 
 // x -> the gate/up B tiles: per group, [k-chunk][rows rounded up to 8][128-byte swizzled
@@ -482,25 +547,51 @@ __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, 
 }
 
 template <int BITS, bool DOWN, int NMAX>
-static int launch_tc(const TcArgs &a, int bound, int sms, cudaStream_t st) {
-  auto k = tc_expert_kernel<BITS, DOWN, NMAX>;
-  constexpr size_t smem = tc_smem<NMAX>();
+static int launch_tc(const TcArgs &a, int bound, int sms, bool pairs, cudaStream_t st) {
+  constexpr size_t smem = tc_smem<NMAX, BITS>();
+  if (!pairs) {
+    auto k = tc_expert_kernel<BITS, DOWN, NMAX, 1>;
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    k<<<bound < sms ? bound : sms, kThreads, smem, st>>>(a, bound);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  auto k = tc_expert_kernel<BITS, DOWN, NMAX, 2>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k<<<bound < sms ? bound : sms, kThreads, smem, st>>>(a, bound);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many clusters as can be resident at once (both CTAs of a cluster share a GPC)
+  int clusters = 0;
+  cfg.gridDim = dim3(2 * (sms / 2));
+  if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters < 1)
+    clusters = sms / 2;
+  const int pairs_total = bound / 2;  // bound is even: every group has an even m-tile count
+  cfg.gridDim = dim3(2 * std::min(clusters, pairs_total));
+  if (cudaLaunchKernelEx(&cfg, k, a, bound) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // NMAX: the smallest supported width >= the largest B row count of any group in the launch
 template <int BITS, bool DOWN>
 static int launch_tc_n(TcArgs a, int rows_max, int kc_gcd, int bound, int sms, cudaStream_t st) {
+  // CTA pairs share activation tiles when every group has an even number of m-tiles
+  const bool pairs = DOWN ? (a.H / 128) % 2 == 0
+                          : (a.LR.inter / 64) % 2 == 0 && (a.LS.inter / 64) % 2 == 0;
   // chunks per copy: code runs of 4 chunks (16 KB at int4) where every K allows it;
   // activation tiles in runs too when they are small (decode), else one chunk per copy
   a.ra = kc_gcd % 4 == 0 ? 4 : (kc_gcd % 2 == 0 ? 2 : 1);
   a.rb = rows_max <= 32 ? a.ra : 1;
-  if (rows_max <= 16) return launch_tc<BITS, DOWN, 16>(a, bound, sms, st);
-  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32>(a, bound, sms, st);
-  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64>(a, bound, sms, st);
-  return launch_tc<BITS, DOWN, 128>(a, bound, sms, st);
+  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32>(a, bound, sms, pairs, st);
+  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64>(a, bound, sms, pairs, st);
+  return launch_tc<BITS, DOWN, 128>(a, bound, sms, pairs, st);
 }
 
 static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
@@ -509,7 +600,7 @@ template <int BITS>
 static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16,
                   const int32_t *perm, const float *tscale, cudaStream_t st, void *mid) {
   DevInfo d = dev_info();
-  if ((long)tc_smem<128>() > d.smem_optin || (long)tc_smem<16>() > d.smem_optin ||
+  if ((long)tc_smem<128, BITS>() > d.smem_optin || (long)tc_smem<32, BITS>() > d.smem_optin ||
       (long)mma_smem_bytes(BITS) > d.smem_optin)
     return MOE_ERR_UNSUPPORTED;
   // enough CTAs to cover the SMs a few times over, whatever the group count
