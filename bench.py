@@ -168,10 +168,13 @@ def traffic_record(kernel):
     d = json.load(open(p)).get(kernel)
     if not d:
         return None
-    src = os.path.join(ROOT, d["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != d["sha256"]:
-        return None
-    return d
+    h = hashlib.sha256()
+    for rel in d["sources"]:
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        h.update(open(src, "rb").read())
+    return d if h.hexdigest() == d["sha256"] else None
 
 
 # ------------------------------------------------------------------ our arm

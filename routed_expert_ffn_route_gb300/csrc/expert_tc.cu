@@ -51,7 +51,11 @@ constexpr int kTraceChunks = 256;
       a.trace[(ev) * kTraceChunks + (c)] = (long long)clock64();          \
   } while (0)
 static long long *g_trace = nullptr;
-extern "C" void moe_trace_set(void *buf) { g_trace = (long long *)buf; }
+long long *g_router_trace = nullptr;  // router selection phases (row 16 of the buffer)
+extern "C" void moe_trace_set(void *buf) {
+  g_trace = (long long *)buf;
+  g_router_trace = buf ? (long long *)buf + 16 * kTraceChunks : nullptr;
+}
 #define MOE_TC_TRACE_R(ev, c) \
   do {                         \
     if (r == 0) MOE_TC_TRACE(ev, c); \
@@ -498,7 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
 // x -> the gate/up B tiles: per group, [k-chunk][rows rounded up to 8][128-byte swizzled
 // row] of fp16 x_t * tscale[t], row = token * P + piece (fp32 x is split into fp16 hi + lo
 // pieces); the padding rows are zero.  Also rscale[row] = 1 / tscale of the row's token.
-// blockIdx.x: group; blockIdx.y strides over the group's (chunk, row, 16-byte) units.
+// One warp per tile row: it reads the token's x row front to back and, for each k-chunk,
+// eight lanes write the chunk's 128-byte line (16 bytes each, at its swizzled slot).
+// blockIdx.x: group; the warps of blockIdx.y stride over the group's rows.
 __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, int is_bf16,
                                                        const int32_t *perm, const float *tscale) {
   const int gi = blockIdx.x;
@@ -506,43 +512,54 @@ __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, 
   const Group g = a.groups[gi];
   const bool sh = g.e == a.E;
   const int rows = a.P * g.n, rows8 = round8(rows), KC = a.H / kKChunk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t *base = const_cast<uint8_t *>(a.xg) + (size_t)g.xrow0 * a.H * 2;
-  auto token = [&](int row) { return sh ? g.pos0 + row / a.P : perm[g.pos0 + row / a.P] / a.k; };
-  if (blockIdx.y == 0)
-    for (int row = threadIdx.x; row < rows8; row += blockDim.x)
-      a.rscale[g.xrow0 + row] = row < rows ? 1.0f / tscale[token(row)] : 0.f;
-  const int units = KC * rows8 * 8;
-  for (int idx = blockIdx.y * blockDim.x + threadIdx.x; idx < units; idx += gridDim.y * blockDim.x) {
-    const int c = idx & 7, row = (idx >> 3) % rows8, kc = idx / (8 * rows8);
-    uint4 *dst = (uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4));
-    if (row >= rows) { *dst = make_uint4(0, 0, 0, 0); continue; }
-    const int tok = token(row), piece = row % a.P;
+  // W warps per group; when the group has fewer rows than that, wpr warps share a row,
+  // each taking every wpr-th group of four k-chunks
+  const int W = gridDim.y * 8, wid = blockIdx.y * 8 + warp;
+  const int wpr = W > rows8 ? W / rows8 : 1, part = wid % wpr;
+  for (int row = wid / wpr; row < rows8; row += W / wpr) {
+    const int c = lane & 7;  // the lane's 16-byte slot of a 128-byte line
+    if (row >= rows) {
+      for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr)
+        *(uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4)) =
+            make_uint4(0, 0, 0, 0);
+      if (lane == 0 && part == 0) a.rscale[g.xrow0 + row] = 0.f;
+      continue;
+    }
+    const int i = row / a.P, piece = row - i * a.P;
+    const int tok = sh ? g.pos0 + i : perm[g.pos0 + i] / a.k;
     const float sc = tscale[tok];
-    const size_t col = (size_t)kc * kKChunk + c * 8;
-    float f[8];
-    if (is_bf16) {
-      const uint4 u = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
-      const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+    if (lane == 0 && part == 0) a.rscale[g.xrow0 + row] = 1.0f / sc;
+#pragma unroll 4
+    for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr) {
+      const size_t col = (size_t)kc * kKChunk + c * 8;
+      float f[8];
+      if (is_bf16) {
+        const uint4 u = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
+        const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+          f[2 * m] = __uint_as_float(q[m] << 16);
+          f[2 * m + 1] = __uint_as_float(q[m] & 0xFFFF0000u);
+        }
+      } else {
+        const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
+        const float4 f0 = src[0], f1 = src[1];
+        f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
+        f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
+      }
+      uint32_t o[4];
 #pragma unroll
       for (int m = 0; m < 4; m++) {
-        f[2 * m] = __uint_as_float(q[m] << 16);
-        f[2 * m + 1] = __uint_as_float(q[m] & 0xFFFF0000u);
+        const float v0 = f[2 * m] * sc, v1 = f[2 * m + 1] * sc;  // exact: sc is a power of two
+        __half2 hv = __floats2half2_rn(v0, v1);
+        if (piece) hv = __floats2half2_rn(v0 - __low2float(hv), v1 - __high2float(hv));
+        o[m] = *(uint32_t *)&hv;
       }
-    } else {
-      const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
-      const float4 f0 = src[0], f1 = src[1];
-      f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
-      f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
+      *(uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
     }
-    uint32_t o[4];
-#pragma unroll
-    for (int m = 0; m < 4; m++) {
-      const float v0 = f[2 * m] * sc, v1 = f[2 * m + 1] * sc;  // exact: sc is a power of two
-      __half2 hv = __floats2half2_rn(v0, v1);
-      if (piece) hv = __floats2half2_rn(v0 - __low2float(hv), v1 - __high2float(hv));
-      o[m] = *(uint32_t *)&hv;
-    }
-    *dst = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -603,8 +620,11 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
   if ((long)tc_smem<128, BITS>() > d.smem_optin || (long)tc_smem<32, BITS>() > d.smem_optin ||
       (long)mma_smem_bytes(BITS) > d.smem_optin)
     return MOE_ERR_UNSUPPORTED;
-  // enough CTAs to cover the SMs a few times over, whatever the group count
-  const int gy = std::max(1, std::min(a.H / kKChunk, (4 * d.sms + W.max_groups - 1) / W.max_groups));
+  // 8 warps per CTA, each with about eight 4-line steps of work; no more CTAs per group
+  // than it takes to cover the SMs a few times over
+  const int rows8_max = round8(a.P * std::min(W.group_n, a.T));
+  const int gy = std::max(1, std::min((rows8_max * (a.H / kKChunk / 4) + 63) / 64,
+                                      (8 * d.sms + W.max_groups - 1) / W.max_groups));
   gather_x_kernel<<<dim3(W.max_groups, gy), 256, 0, st>>>(a, x, is_bf16, perm, tscale);
   const int mt_s = a.LS.inter / 64, mt_r = a.LR.inter / 64, mt_d = a.H / 128;
   const int bound_gu = a.ns * mt_s + (W.max_groups - a.ns) * mt_r;

@@ -93,7 +93,9 @@ struct Ctrl {
   int status;      // moe_status recorded on the device (0 = OK)
   int detail;      // where it was recorded (kernel id)
   int n_groups;    // groups written by the permute kernel (shared groups included)
-  int pad[61];
+  int pad0;
+  int gemv_done[32];  // router GEMV: H-slice CTAs finished, per block of 8 experts
+  int pad[28];
 };
 
 constexpr int kRouterHS = 8;   // H splits of the small-T router GEMV
@@ -133,7 +135,8 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   uint64_t hg_rows = W.tc ? (uint64_t)W.rows + 7ull * W.max_groups : 0;
   uint64_t o = 0;
   W.ctrl = o; o += 256;
-  W.partials = o; o = align_up(o + (uint64_t)kRouterHS * T * c.n_experts * 4, 256);
+  // router partial logits [HS][T][E], then per-slice max |x| [HS][T]
+  W.partials = o; o = align_up(o + (uint64_t)kRouterHS * T * (c.n_experts + 1) * 4, 256);
   W.offsets = o; o = align_up(o + (uint64_t)(c.n_experts + 1) * 4, 256);
   W.perm = o; o = align_up(o + (uint64_t)tk * 4, 256);
   W.slot_pos = o; o = align_up(o + (uint64_t)tk * 4, 256);

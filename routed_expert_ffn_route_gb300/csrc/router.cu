@@ -22,6 +22,18 @@
 
 namespace moe {
 
+#ifdef MOE_TRACE
+extern long long *g_router_trace;
+#define MOE_RT_TRACE(i)                                      \
+  do {                                                       \
+    if (t == 0 && lane == 0 && rtrace) rtrace[i] = clock64(); \
+  } while (0)
+#else
+#define MOE_RT_TRACE(i) \
+  do {                  \
+  } while (0)
+#endif
+
 __device__ __forceinline__ void check_header(const uint8_t *packed, const moe_layer_config &c,
                                              Ctrl *ctrl) {
   const PackHeader *h = (const PackHeader *)packed;
@@ -36,26 +48,51 @@ template <int TM>
 __global__ void __launch_bounds__(256) router_gemv_kernel(moe_layer_config c, const uint8_t *packed,
                                                           const float *wr, const void *x,
                                                           int is_bf16, int T, float *partials,
-                                                          Ctrl *ctrl) {
+                                                          Ctrl *ctrl, float *xmax) {
   extern __shared__ float xs[];  // [T][HL]
   const int H = c.hidden, E = c.n_experts;
   const int HL = H / kRouterHS;
   const int hs = blockIdx.y;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) check_header(packed, c, ctrl);
-  for (int i = threadIdx.x; i < T * HL; i += blockDim.x) {
-    int t = i / HL, cc = i % HL;
-    long src = (long)t * H + (long)hs * HL + cc;
-    xs[i] = is_bf16 ? bf16_to_f32(((const uint16_t *)x)[src]) : ((const float *)x)[src];
+  // 8 elements per thread and step (HL is a multiple of 16), unrolled so the loads overlap
+#pragma unroll 4
+  for (int i = 8 * threadIdx.x; i < T * HL; i += 8 * blockDim.x) {
+    const int t = i / HL, cc = i - t * HL;
+    const long src = (long)t * H + (long)hs * HL + cc;
+    if (is_bf16) {
+      const uint4 u = *(const uint4 *)((const uint16_t *)x + src);
+      const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        xs[i + 2 * m] = __uint_as_float(q[m] << 16);
+        xs[i + 2 * m + 1] = __uint_as_float(q[m] & 0xFFFF0000u);
+      }
+    } else {
+      const float4 f0 = *(const float4 *)((const float *)x + src);
+      const float4 f1 = *(const float4 *)((const float *)x + src + 4);
+      *(float4 *)(xs + i) = f0;
+      *(float4 *)(xs + i + 4) = f1;
+    }
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the first expert block also reduces max |x| over its H slice, per token: the
+  // selection kernel combines the slices into the token's activation scale
+  if (xmax && blockIdx.x == 0)
+    for (int t = warp; t < T; t += 8) {
+      float m = 0.f;
+      for (int i = lane; i < HL; i += 32) m = fmaxf(m, fabsf(xs[t * HL + i]));
+      m = warp_max(m);
+      if (lane == 0) xmax[hs * T + t] = m;
+    }
   const int e = blockIdx.x * 8 + warp;
-  if (e >= E) return;
-  const float4 *wrow = (const float4 *)(wr + (long)e * H + (long)hs * HL);
+  const bool live = e < E;  // no early return: the block synchronises below
+  const float4 *wrow = (const float4 *)(wr + (long)(live ? e : 0) * H + (long)hs * HL);
   float acc[TM];
 #pragma unroll
   for (int t = 0; t < TM; t++) acc[t] = 0.f;
-  for (int q = lane; q < HL / 4; q += 32) {
+#pragma unroll 8
+  for (int q = lane; live && q < HL / 4; q += 32) {  // unrolled: the row's loads in flight
     float4 wv = __ldg(wrow + q);
 #pragma unroll
     for (int t = 0; t < TM; t++) {
@@ -72,7 +109,30 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(moe_layer_config c, co
   for (int t = 0; t < TM; t++) {
     if (t < T) {
       float s = warp_sum(acc[t]);
-      if (lane == 0) partials[((long)hs * T + t) * E + e] = s;
+      if (lane == 0 && live) partials[((long)hs * T + t) * E + e] = s;
+    }
+  }
+  // The last of the kRouterHS H-slice blocks of this expert block adds the slices' partial
+  // logits in slice order into slice 0, so the selection kernel reads one value per logit.
+  __shared__ int last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this block's partials are visible before it is counted
+    last = atomicAdd(&ctrl->gemv_done[blockIdx.x], 1) == kRouterHS - 1;
+  }
+  __syncthreads();
+  if (last) {
+    __threadfence();
+    for (int i = threadIdx.x; i < 8 * T; i += blockDim.x) {
+      const int t = i >> 3, ee = blockIdx.x * 8 + (i & 7);
+      if (ee >= E) continue;
+      float v[kRouterHS];
+#pragma unroll
+      for (int h = 0; h < kRouterHS; h++) v[h] = __ldcg(partials + ((long)h * T + t) * E + ee);
+      float sum = 0.f;
+#pragma unroll
+      for (int h = 0; h < kRouterHS; h++) sum += v[h];
+      partials[(long)t * E + ee] = sum;
     }
   }
 }
@@ -223,6 +283,20 @@ __device__ __forceinline__ Cand warp_best(Cand c) {
 
 constexpr int kMaxV = 8;  // experts per lane (E <= 256)
 
+// Order-preserving map of a float (not NaN) to an unsigned key: a > b iff key(a) > key(b).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// The warp's best (score, index) pair: the largest score, ties to the lowest index, using
+// two hardware warp reductions (index < 65536; lanes without a candidate pass key 0).
+__device__ __forceinline__ int warp_argmax(uint32_t key, int idx) {
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  const uint32_t inv = __reduce_max_sync(0xffffffffu, key == kmax ? 0xFFFFu - (uint32_t)idx : 0u);
+  return (int)(0xFFFFu - inv);
+}
+
 // 2^e with max_abs * 2^e in [2^14, 2^15): x_t * 2^e converts to fp16 without loss for every
 // element that bf16 holds within 2^-24 of the token's largest (fp16 keeps 11 significant
 // bits over that range).  A zero or non-finite maximum gets 1.
@@ -238,17 +312,24 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
                                                           const float *partials, int hsplits,
                                                           int T, int32_t *ids, float *w,
                                                           Ctrl *ctrl, const void *x, int is_bf16,
-                                                          float *tscale) {
+                                                          float *tscale, const float *xmax,
+                                                          long long *rtrace) {
   __shared__ float csm[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
+  MOE_RT_TRACE(0);
   const int E = c.n_experts, k = c.top_k;
   const bool grouped = c.router == MOE_ROUTER_SIGMOID_GROUPED;
-  if (tscale) {
+  if (tscale && xmax) {  // max |x_t| from the router GEMV's kRouterHS H slices
+    float m = lane < kRouterHS ? xmax[lane * T + t] : 0.f;
+    m = warp_max(m);
+    if (lane == 0) tscale[t] = token_scale(m);
+  } else if (tscale) {
     const int H = c.hidden;
     float m = 0.f;
-    for (int i = 8 * lane; i < H; i += 256) {
+#pragma unroll 8
+    for (int i = 8 * lane; i < H; i += 256) {  // unrolled: the row's loads in flight together
       if (is_bf16) {
         const uint4 u = *(const uint4 *)((const uint16_t *)x + (long)t * H + i);
         const uint32_t q[4] = {u.x, u.y, u.z, u.w};
@@ -266,17 +347,20 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
     m = warp_max(m);
     if (lane == 0) tscale[t] = token_scale(m);
   }
+  MOE_RT_TRACE(6);
   float sel[kMaxV], wsrc[kMaxV];
   float mx = -INFINITY;
   // the H-split partial logits, all loaded before they are added (in split order)
-  float part[kMaxV][kRouterHS];
+  float part[kMaxV][kRouterHS], bv[kMaxV];  // ... and the selection biases, loaded with them
 #pragma unroll
-  for (int v = 0; v < kMaxV; v++)
+  for (int v = 0; v < kMaxV; v++) {
+    const int e = lane + 32 * v;
+    bv[v] = (grouped && e < E) ? bias[e] : 0.f;
 #pragma unroll
-    for (int hs = 0; hs < kRouterHS; hs++) {
-      const int e = lane + 32 * v;
+    for (int hs = 0; hs < kRouterHS; hs++)
       part[v][hs] = (e < E && hs < hsplits) ? partials[((long)hs * T + t) * E + e] : 0.f;
-    }
+  }
+  bool nonfinite = false;
 #pragma unroll
   for (int v = 0; v < kMaxV; v++) {
     int e = lane + 32 * v;
@@ -286,15 +370,16 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
 #pragma unroll
       for (int hs = 0; hs < kRouterHS; hs++)
         if (hs < hsplits) l += part[v][hs];
-      if (!isfinite(l)) {
-        // a non-finite logit: report it, and keep the selection total and in range
-        record_status(ctrl, MOE_ERR_NUMERIC, kKTopk);
+      if (!isfinite(l)) {  // keep the selection total and in range; reported below
+        nonfinite = true;
         l = -INFINITY;
       }
     }
     sel[v] = l;
     mx = fmaxf(mx, l);
   }
+  if (nonfinite) record_status(ctrl, MOE_ERR_NUMERIC, kKTopk);  // after all loads were issued
+  MOE_RT_TRACE(1);
   float sum_all = 1.f;
   if (!grouped) {
     mx = warp_max(mx);
@@ -313,7 +398,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
       if (e < E) {
         float sg = 1.0f / (1.0f + expf(-sel[v]));
         wsrc[v] = sg;
-        sel[v] = sg + bias[e];
+        sel[v] = sg + bv[v];
         if (isnan(sel[v])) sel[v] = -INFINITY;
         csm[warp][e] = sel[v];
       } else {
@@ -321,6 +406,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
       }
     }
   }
+  MOE_RT_TRACE(2);
   unsigned allowed_groups = 0xffffffffu;
   int gs = E;
   if (grouped) {
@@ -339,31 +425,45 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
       gc.e = lane;
     }
     allowed_groups = 0;
+    uint32_t gkey = lane < G ? order_key(gc.s) : 0u;
     for (int j = 0; j < c.topk_group; j++) {
-      Cand b = warp_best(gc);
-      allowed_groups |= 1u << b.e;
-      if (lane == b.e) gc.s = -INFINITY, gc.e = 1 << 30;
+      const int b = warp_argmax(gkey, lane);
+      allowed_groups |= 1u << b;
+      if (lane == b) gkey = 0u;
     }
   }
-  unsigned taken = 0;
+  MOE_RT_TRACE(3);
+  // this lane's candidates (bit v: expert lane + 32 v) in the kept groups
+  unsigned avail = 0;
+#pragma unroll
+  for (int v = 0; v < kMaxV; v++) {
+    const int e = lane + 32 * v;
+    if (e < E && ((allowed_groups >> (e / gs)) & 1)) avail |= 1u << v;
+  }
   float my_w = 0.f, wsum = 0.f;
   int my_id = 0;
-  for (int j = 0; j < k; j++) {
-    Cand best{-INFINITY, 1 << 30, 0.f};
+  uint32_t skey[kMaxV];  // selection keys (0: not a candidate)
 #pragma unroll
-    for (int v = 0; v < kMaxV; v++) {
-      int e = lane + 32 * v;
-      bool ok = e < E && !((taken >> v) & 1) && ((allowed_groups >> (e / gs)) & 1);
-      if (ok) {
-        Cand cd{sel[v], e, wsrc[v]};
-        if (better(cd, best)) best = cd;
-      }
-    }
-    Cand b = warp_best(best);
-    if ((b.e & 31) == lane && b.e < E) taken |= 1u << (b.e >> 5);
-    wsum += b.w;
-    if (lane == j) { my_id = b.e; my_w = b.w; }
+  for (int v = 0; v < kMaxV; v++) skey[v] = order_key(sel[v]);
+  for (int j = 0; j < k; j++) {
+    // this lane's best remaining candidate: largest key, then lowest v (= lowest expert)
+    uint32_t bk = 0u;
+    int bvx = 0;
+#pragma unroll
+    for (int v = kMaxV - 1; v >= 0; v--)
+      if (((avail >> v) & 1) && skey[v] >= bk) { bk = skey[v]; bvx = v; }
+    const int e_best = warp_argmax(bk, lane + 32 * bvx);
+    const int owner = e_best & 31, vb = e_best >> 5;
+    float wsel = 0.f;
+#pragma unroll
+    for (int v = 0; v < kMaxV; v++)
+      if (v == vb) wsel = wsrc[v];
+    const float wb = __shfl_sync(0xffffffffu, wsel, owner);
+    if (lane == owner) avail &= ~(1u << vb);
+    wsum += wb;
+    if (lane == j) { my_id = e_best; my_w = wb; }
   }
+  MOE_RT_TRACE(4);
   if (lane < k) {
     float v;
     if (c.norm_topk) v = my_w / wsum;
@@ -371,6 +471,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(moe_layer_config c, co
     ids[(long)t * k + lane] = my_id;
     w[(long)t * k + lane] = v * c.routed_scaling_factor;
   }
+  MOE_RT_TRACE(5);
 }
 
 int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *x, moe_dtype dt,
@@ -382,23 +483,23 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
   Ctrl *ctrl = (Ctrl *)(ws + W.ctrl);
   int is_bf16 = dt == MOE_DT_BF16;
   int hsplits;
-  if (T <= 16 && (size_t)T * (c.hidden / kRouterHS) * 4 <= 96 * 1024) {
-    hsplits = kRouterHS;
+  // per-slice max |x| of the GEMV path (after the partial logits in the same region)
+  float *xmax = W.tc ? partials + (size_t)kRouterHS * T * c.n_experts : nullptr;
+  const bool gemv = T <= 16 && (size_t)T * (c.hidden / kRouterHS) * 4 <= 96 * 1024;
+  if (gemv) {
+    hsplits = 1;  // the GEMV adds its H slices into slice 0 itself
     dim3 grid((c.n_experts + 7) / 8, kRouterHS);
     size_t smem = (size_t)T * (c.hidden / kRouterHS) * 4;
-    if (smem > 48 * 1024) {
-      cudaFuncSetAttribute(router_gemv_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-      cudaFuncSetAttribute(router_gemv_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-    }
-#define GEMV(TM) router_gemv_kernel<TM><<<grid, 256, smem, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl)
-    if (T <= 1) GEMV(1);
-    else if (T <= 2) GEMV(2);
-    else if (T <= 4) GEMV(4);
-    else if (T <= 8) GEMV(8);
-    else GEMV(16);
-#undef GEMV
+    // the dynamic x slice plus the block's static flag may pass the 48 KB default
+    auto launch = [&](auto k) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      k<<<grid, 256, smem, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl, xmax);
+    };
+    if (T <= 1) launch(router_gemv_kernel<1>);
+    else if (T <= 2) launch(router_gemv_kernel<2>);
+    else if (T <= 4) launch(router_gemv_kernel<4>);
+    else if (T <= 8) launch(router_gemv_kernel<8>);
+    else launch(router_gemv_kernel<16>);
   } else {
     // 128 x 128 tiles for large T, 64 x 64 below; H split (partial sums added in order by
     // the selection kernel) until the grid covers the SMs twice
@@ -420,7 +521,13 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
   const float *bias = (const float *)(packed + P.router_b_off);
   float *tscale = W.tc ? (float *)(ws + W.tscale) : nullptr;
   router_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(c, bias, partials, hsplits, T, ids, w, ctrl, x,
-                                                  is_bf16, tscale);
+                                                  is_bf16, tscale, gemv ? xmax : nullptr,
+#ifdef MOE_TRACE
+                                                  g_router_trace
+#else
+                                                  nullptr
+#endif
+  );
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
