@@ -152,8 +152,11 @@ int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const voi
 /* moe_layer_forward with stage timing: records the caller's CUDA events (cudaEvent_t
  * passed as void*) on `stream` around the stages, events[0] before the first kernel and
  * events[i+1] after stage i, for the stages 0 router (logits + top-k), 1 permutation,
- * 2 Q8_0 activation encoding (empty unless act_q8_0), 3 gate/up + SwiGLU, 4 down
- * projection, 5 combine.  n_events must be >= 7.  Same results as moe_layer_forward. */
+ * 2 activation encoding (Q8_0 codes with act_q8_0, else the fp16 tensor-core tiles),
+ * 3 gate/up + SwiGLU, 4 down projection, 5 combine.  n_events must be >= 7.  Same results
+ * as moe_layer_forward.  The call may be captured into a CUDA graph: while the stream is
+ * capturing, the events are recorded as graph nodes (cudaEventRecordExternal), so each
+ * replay records them. */
 int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, const void *x,
                             moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
                             size_t ws_bytes, void *const *events, int n_events, void *stream);

@@ -42,7 +42,7 @@ EXPORTED = [
 ]
 
 # stages bracketed by the events of moe_layer_forward_timed
-STAGES = ["router", "permute", "q8_encode", "gate_up", "down", "combine"]
+STAGES = ["router", "permute", "act_encode", "gate_up", "down", "combine"]
 
 
 class MoEError(RuntimeError):

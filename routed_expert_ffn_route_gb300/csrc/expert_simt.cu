@@ -336,7 +336,7 @@ static int run_experts(const moe_layer_config &c, const ExpertArgs &a, const WsL
                       : (size_t)GN * a.Imax * 4;
   int r = launch_persistent(gate_up_kernel<BITS, GN, Q8>, smem_gu, bound_gu, a, st);
   if (r) return r;
-  if (mid && cudaEventRecord((cudaEvent_t)mid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mid && record_stage_event(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
   return launch_persistent(down_kernel<BITS, GN, Q8>, smem_dn, bound_dn, a, st);
 }
 
@@ -353,8 +353,9 @@ static int run_gn(const moe_layer_config &c, const ExpertArgs &a, const WsLayout
 
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                   void *mid) {
-  if (W.tc) return launch_experts_tc(c, packed, x, dt, T, ws, W, st, mid);
+                   void *act, void *mid) {
+  if (W.tc) return launch_experts_tc(c, packed, x, dt, T, ws, W, st, act, mid);
+  if (act && record_stage_event(act, st) != cudaSuccess) return MOE_ERR_CUDA;
   ExpertArgs a = make_args(c, packed, x, dt, T, ws, W);
   if (c.act_q8_0) return run_gn<8, true>(c, a, W, mid, st);
   switch (c.weight_bits) {

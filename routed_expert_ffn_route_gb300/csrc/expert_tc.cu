@@ -615,7 +615,8 @@ static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
 
 template <int BITS>
 static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16,
-                  const int32_t *perm, const float *tscale, cudaStream_t st, void *mid) {
+                  const int32_t *perm, const float *tscale, cudaStream_t st, void *act,
+                  void *mid) {
   DevInfo d = dev_info();
   if ((long)tc_smem<128, BITS>() > d.smem_optin || (long)tc_smem<32, BITS>() > d.smem_optin ||
       (long)mma_smem_bytes(BITS) > d.smem_optin)
@@ -626,6 +627,7 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
   const int gy = std::max(1, std::min((rows8_max * (a.H / kKChunk / 4) + 63) / 64,
                                       (8 * d.sms + W.max_groups - 1) / W.max_groups));
   gather_x_kernel<<<dim3(W.max_groups, gy), 256, 0, st>>>(a, x, is_bf16, perm, tscale);
+  if (act && record_stage_event(act, st) != cudaSuccess) return MOE_ERR_CUDA;
   const int mt_s = a.LS.inter / 64, mt_r = a.LR.inter / 64, mt_d = a.H / 128;
   const int bound_gu = a.ns * mt_s + (W.max_groups - a.ns) * mt_r;
   const int bound_dn = W.max_groups * mt_d;
@@ -638,7 +640,7 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
               ? launch_experts_mma(BITS, false, a, rows_gu, a.H / kKChunk, bound_gu, d.sms, st)
               : launch_tc_n<BITS, false>(a, rows_gu, a.H / kKChunk, bound_gu, d.sms, st);
   if (r) return r;
-  if (mid && cudaEventRecord((cudaEvent_t)mid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (mid && record_stage_event(mid, st) != cudaSuccess) return MOE_ERR_CUDA;
   TcArgs ad = a;
   ad.trace = nullptr;  // traces (development builds) cover the gate/up kernel
   const int kc_dn = gcd_i(a.LR.inter / kKChunk, a.LS.inter / kKChunk);
@@ -649,7 +651,7 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
 
 int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const void *x,
                       moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                      void *mid) {
+                      void *act, void *mid) {
   PackLayout P = pack_layout(c);
   TcArgs a{};
   a.routed = packed + P.experts_off;
@@ -679,9 +681,9 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   const int32_t *perm = (const int32_t *)(ws + W.perm);
   const int is_bf16 = dt == MOE_DT_BF16;
   switch (c.weight_bits) {
-    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, mid);
-    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, mid);
-    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, mid);
+    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, act, mid);
+    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, act, mid);
+    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, act, mid);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

@@ -221,7 +221,7 @@ static int forward_impl(const moe_layer_config *cfg, const void *packed, const v
   uint8_t *wsb = (uint8_t *)ws;
   const uint8_t *pk = (const uint8_t *)packed;
   auto mark = [&](int i) {
-    return ev ? cudaEventRecord((cudaEvent_t)ev[i], st) == cudaSuccess : true;
+    return ev ? record_stage_event(ev[i], st) == cudaSuccess : true;
   };
   if (cudaMemsetAsync(ws, 0, sizeof(Ctrl), st) != cudaSuccess || !mark(0)) return MOE_ERR_CUDA;
   if ((r = launch_router(*cfg, pk, x, dtype, T, ids, w, wsb, W, st))) return r;
@@ -229,8 +229,11 @@ static int forward_impl(const moe_layer_config *cfg, const void *packed, const v
   if ((r = launch_permute(*cfg, T, ids, wsb, W, st))) return r;
   if (!mark(2)) return MOE_ERR_CUDA;
   if (cfg->act_q8_0 && (r = launch_quant_x(*cfg, x, dtype, T, wsb, W, st))) return r;
-  if (!mark(3)) return MOE_ERR_CUDA;
-  if ((r = launch_experts(*cfg, pk, x, dtype, T, wsb, W, st, ev ? ev[4] : nullptr))) return r;
+  // stage 2 ends when the activations are encoded: Q8_0 codes, or the tensor-core path's
+  // fp16 tiles (gathered inside launch_experts)
+  if ((r = launch_experts(*cfg, pk, x, dtype, T, wsb, W, st, ev ? ev[3] : nullptr,
+                          ev ? ev[4] : nullptr)))
+    return r;
   if (!mark(5)) return MOE_ERR_CUDA;
   if ((r = launch_combine(*cfg, T, w, out, wsb, W, st))) return r;
   return mark(6) ? MOE_OK : MOE_ERR_CUDA;

@@ -172,6 +172,17 @@ __host__ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; 
 __host__ __device__ __forceinline__ int round8(int v) { return (v + 7) & ~7; }
 
 // ---------------------------------------------------------------- launch helpers
+// Record a caller's timing event on `st`.  While `st` is being captured into a CUDA graph
+// the record becomes a graph node (replays record it), so stage timings also work for
+// graph-launched forwards.
+static inline cudaError_t record_stage_event(void *ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return cudaErrorUnknown;
+  return cs == cudaStreamCaptureStatusActive
+             ? cudaEventRecordWithFlags((cudaEvent_t)ev, st, cudaEventRecordExternal)
+             : cudaEventRecord((cudaEvent_t)ev, st);
+}
+
 struct DevInfo {
   int sms;
   int smem_optin;
@@ -188,11 +199,12 @@ int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T
                    const WsLayout &W, cudaStream_t st);
 int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const void *x,
                       moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                      void *mid);
-// mid_event (a cudaEvent_t or null) is recorded between the gate/up and down launches
+                      void *act, void *mid);
+// act_event / mid_event (cudaEvent_t or null) are recorded after the activation encoding
+// (tensor-core path: the fp16 tile gather) and between the gate/up and down launches
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                   void *mid_event);
+                   void *act_event, void *mid_event);
 int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
 int launch_pack_expert(const moe_layer_config &c, const ExpertLayout &L, const int8_t *gate,
