@@ -72,7 +72,8 @@ def dist_init(n):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
@@ -90,9 +91,14 @@ def allmax(v, ws):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([float(v)], device="cuda")
+    t = torch.tensor([float(v)], device="cuda" if torch.cuda.is_available() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tokens_per_s(tokens_per_rank, ws, rank_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's device time."""
+    return tokens_per_rank * ws / (allmax(rank_ms, ws) / 1e3)
 
 
 # ------------------------------------------------------------------ clocks
@@ -307,7 +313,7 @@ def run_ours(a, rank, ws_n, local):
     total_ms = sum(fwd_ms.values())
     total_ms_max = allmax(total_ms, ws_n)
     tokens = a.steps * sum(TS) * ws_n
-    value = tokens / (total_ms_max / 1e3)
+    value = aggregate_tokens_per_s(a.steps * sum(TS), ws_n, total_ms)
 
     # e2e: pinned host buffers, copies inside the timed region
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
