@@ -58,6 +58,8 @@ def args_():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true",
+                    help="skip the 8-layer stack (prefill T=4096 + 256 decode steps)")
     ap.add_argument("--T", default=",".join(map(str, TS)),
                     help="token counts of one step (default: the headline 1,16,2048)")
     return ap.parse_args()
@@ -410,9 +412,110 @@ def run_ours(a, rank, ws_n, local):
         "clocks": clk,
         "wall_s_timed_region": round(t_wall, 3),
     }
+    if not a.no_stack:
+        line["stack"] = run_stack(a, rank, ws_n, pk)
     if rank == 0 and ws_n == 1 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, seed, ntok=4, reps=6)
     return line
+
+
+# ------------------------------------------------------------------ the stacked layers
+
+def zipf_beta():
+    for line in open(os.path.join(ROOT, "tests", "golden", "zipf_beta.txt")):
+        if line.startswith("beta "):
+            return float(line.split()[1])
+    raise RuntimeError("tests/golden/zipf_beta.txt has no beta")
+
+
+def run_stack(a, rank, ws_n, pk):
+    """8 DeepSeek-V3-shaped layers, all 257 experts of each resident (~39 GB), router bias
+    Zipf(1.1)-skewed: one T = 4096 prefill through the stack, then 256 sequential T = 1
+    decode steps (each a fresh seeded token).  Each is a CUDA graph of the stack's C-ABI
+    calls (layer forward + residual/RMSNorm step per layer)."""
+    import numpy as np
+    import torch
+
+    import gen
+    from gen.device import build_packed_layer, hidden_to_device
+    from routed_expert_ffn_route_gb300.stack import Stack
+
+    L, T_pre, steps, seed = 8, 4096, 256, 0
+    s = gen.spec("dsv3")
+    beta = zipf_beta()
+    t0 = time.perf_counter()
+    layers = [build_packed_layer(s, seed, l, "cuda", bias=gen.zipf_bias(s, seed, l, beta))
+              for l in range(L)]
+    pack_s = time.perf_counter() - t0
+    st = Stack(layers, T_pre)
+    x, bits = gen.hidden_states(s, seed + 1000 * rank, 70, T_pre)
+    x_pre = hidden_to_device(s, x, bits)
+    xd, bd = gen.hidden_states(s, seed + 1000 * rank, 71, steps)
+    x_dec = hidden_to_device(s, xd, bd)
+    x_one = torch.empty((1, s.hidden), dtype=torch.bfloat16, device="cuda")
+    st.forward(x_pre)
+    x_one.copy_(x_dec[:1])
+    st.forward(x_one)
+    st.status()
+    torch.cuda.synchronize()
+    g_pre, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pre):
+        st.forward(x_pre)
+    with torch.cuda.graph(g_dec):
+        st.forward(x_one)
+    torch.cuda.synchronize()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    # prefill: 3 replays after one warm-up, L2 flushed before each
+    g_pre.replay()
+    pre_ms = []
+    for _ in range(3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g_pre.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        pre_ms.append(e0.elapsed_time(e1))
+    ids_pre = [i[:T_pre].cpu().numpy() for i in st.ids]
+    # decode: 256 sequential steps, each step's token copied in, then the stack replayed
+    uniq = []
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record()
+    for i in range(steps):
+        x_one.copy_(x_dec[i:i + 1])
+        g_dec.replay()
+    ev[1].record()
+    torch.cuda.synchronize()
+    dec_ms = ev[0].elapsed_time(ev[1]) / steps
+    for i in range(8):  # unique experts per decode step, from a few untimed steps
+        x_one.copy_(x_dec[i:i + 1])
+        g_dec.replay()
+        torch.cuda.synchronize()
+        uniq.append(sum(int(np.unique(l[:1].cpu().numpy()).size) for l in st.ids))
+    st.status()
+    pre = statistics.median(pre_ms)
+    fl = L * layer_flops(s, T_pre)
+    dec_bytes = (statistics.mean(uniq) + L * s.n_shared) * expert_bytes(s, s.inter)
+    skew = [float(np.bincount(l.ravel(), minlength=s.n_experts).max() / T_pre) for l in ids_pre]
+    out = {
+        "layers": L, "zipf_beta": beta, "resident_expert_gb": round(L * (s.n_experts + s.n_shared)
+                                                                    * expert_bytes(s, s.inter) / 1e9, 2),
+        "pack_s": round(pack_s, 1),
+        "prefill": {"T": T_pre, "ms": round(pre, 3), "tokens_per_s": round(T_pre / (pre / 1e3), 1),
+                    "bf16_frac_of_measured_sustained": round(fl / (pre / 1e3) / 1e12 / pk["bf16_sus"], 4),
+                    "max_expert_share_per_layer": [round(v, 3) for v in skew]},
+        "decode": {"steps": steps, "ms_per_step": round(dec_ms, 4),
+                   "tokens_per_s": round(1e3 / dec_ms, 1),
+                   "unique_expert_bytes_per_step": int(dec_bytes),
+                   "hbm_frac_of_measured": round(dec_bytes / (dec_ms / 1e3) / 1e9 / pk["hbm"], 4),
+                   "l2": "not flushed between steps (each step streams ~1.4 GB of experts)"},
+        "timing": "CUDA graphs of the stack's C-ABI calls; prefill median of 3 replays after an "
+                  "L2 flush; decode = events around 256 sequential replays",
+    }
+    del g_pre, g_dec, st, layers
+    torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------------ the oracle (CPU baseline)

@@ -32,7 +32,7 @@ __all__ = [
     "lowbias32_np", "draws_np", "draws_torch",
     "expert_codes", "expert_codes_torch", "expert_scales",
     "router_weights", "router_bias", "hidden_states", "bf16_round_bits",
-    "expert_rows_cols", "zipf_bias",
+    "expert_rows_cols", "zipf_bias", "zipf_rank",
 ]
 
 M32 = 0xFFFFFFFF
@@ -250,11 +250,17 @@ def router_bias(s: LayerSpec, seed: int, layer: int = 0):
     return (s.bias_std * z).astype(np.float32)
 
 
-def zipf_bias(s: LayerSpec, seed: int, layer: int, beta: float, zipf_s: float = 1.1) -> np.ndarray:
-    """Zipf-shaped router bias: b_e = -beta * zipf_s * ln(rank_e), rank a seeded permutation 1..E."""
+def zipf_rank(s: LayerSpec, seed: int, layer: int) -> np.ndarray:
+    """The Zipf rank (1..E) of every expert of a layer: a seeded permutation."""
     h = draws_np(seed, TAG["zipf_perm"], _sub(layer, 0), 0, s.n_experts)
     rank = np.empty(s.n_experts, dtype=np.int64)
     rank[np.argsort(h, kind="stable")] = np.arange(1, s.n_experts + 1)
+    return rank
+
+
+def zipf_bias(s: LayerSpec, seed: int, layer: int, beta: float, zipf_s: float = 1.1) -> np.ndarray:
+    """Zipf-shaped router bias: b_e = -beta * zipf_s * ln(rank_e), rank a seeded permutation 1..E."""
+    rank = zipf_rank(s, seed, layer)
     return (-beta * zipf_s * np.log(rank.astype(np.float64))).astype(np.float32)
 
 

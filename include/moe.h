@@ -216,6 +216,17 @@ int moe_debug_block_dots(const moe_layer_config *cfg, const void *packed, int ex
  * (read it with moe_read_status).  Exercises the timeout path without a fault. */
 int moe_debug_wait_timeout(void *ws, size_t ws_bytes, int iterations, void *stream);
 
+/* The step between two stacked layers ("colibrì 深度拆解" §4.3: a layer's merged output
+ * feeds the next layer; the stacking arithmetic is this library's reading): for every
+ * token t, resid[t] = x0[t] when x0 is given (the stack's input, bf16; add is then
+ * ignored), else resid[t] += add[t] (fp32, in place; add may be NULL), then
+ * x_next[t] = bf16(resid[t] / sqrt(mean(resid[t]^2) + eps)), unweighted RMSNorm rounded to
+ * nearest: the next layer's input.  resid, add [T][H] fp32, x0 and x_next [T][H] bf16
+ * (uint16 bit patterns) are device pointers, 16-byte aligned; H a multiple of 8; eps >= 0.
+ * Returns MOE_ERR_INVALID_ARG before any launch when an argument is out of range. */
+int moe_residual_rmsnorm(int T, int H, float *resid, const float *add, const uint16_t *x0,
+                         float eps, uint16_t *x_next, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

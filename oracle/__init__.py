@@ -80,6 +80,7 @@ def _bind(lib):
     lib.orc_block_dot.argtypes = [P, P]
     for f in ("orc_pack_int4", "orc_unpack_int4", "orc_pack_int2", "orc_unpack_int2"):
         getattr(lib, f).argtypes = [P, C.c_size_t, P]
+    lib.orc_residual_rmsnorm.argtypes = [C.c_int, C.c_int, P, P, C.c_double, P]
     return lib
 
 
@@ -249,3 +250,13 @@ pack_int4 = _packer("orc_pack_int4", 2)
 pack_int2 = _packer("orc_pack_int2", 4)
 unpack_int4 = _unpacker("orc_unpack_int4")
 unpack_int2 = _unpacker("orc_unpack_int2")
+
+
+def residual_rmsnorm(r: np.ndarray, add=None, eps: float = 1e-6):
+    """Stack step: r += add (in place on a copy), x = bf16(RMSNorm(r)).  -> (r, x) fp64."""
+    r = np.array(r, dtype=np.float64, order="C", copy=True)
+    T, H = r.shape
+    a = None if add is None else np.ascontiguousarray(add, dtype=np.float64)
+    xn = np.empty_like(r)
+    load().orc_residual_rmsnorm(T, H, _p(r), None if a is None else _p(a), float(eps), _p(xn))
+    return r, xn

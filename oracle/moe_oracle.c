@@ -371,3 +371,32 @@ void orc_pack_int2(const int8_t *q, size_t n, uint8_t *out) {
 void orc_unpack_int2(const uint8_t *p, size_t n, int8_t *q) {
   for (size_t i = 0; i < n; i++) q[i] = sext((p[i / 4] >> (6 - 2 * (int)(i % 4))) & 3, 2);
 }
+
+/* Round an fp64 value to bf16 (8 significant bits), to nearest, ties to even; returns the
+ * bf16 value exactly as a double.  Values beyond the bf16 range become +-inf. */
+static double round_bf16(double v) {
+  if (v == 0.0 || isnan(v) || isinf(v)) return v;
+  int e;
+  double m = frexp(v, &e);              /* v = m * 2^e, 0.5 <= |m| < 1 */
+  if (e < -125) {                       /* bf16 subnormals: fixed step 2^-133 */
+    double q = nearbyint(ldexp(v, 133)); /* current rounding mode: to nearest even */
+    return ldexp(q, -133);
+  }
+  double q = nearbyint(ldexp(m, 8));    /* 8 significant bits */
+  double r = ldexp(q, e - 8);
+  if (fabs(r) >= 0x1.ffp127 * (1.0 + 0x1p-9)) return v > 0 ? INFINITY : -INFINITY;
+  return r;
+}
+
+void orc_residual_rmsnorm(int T, int H, double *r, const double *add, double eps,
+                          double *xn) {
+  for (int t = 0; t < T; t++) {
+    double *rt = r + (size_t)t * H;
+    if (add)
+      for (int h = 0; h < H; h++) rt[h] += add[(size_t)t * H + h];
+    double ss = 0.0;
+    for (int h = 0; h < H; h++) ss += rt[h] * rt[h];
+    const double inv = 1.0 / sqrt(ss / H + eps);
+    for (int h = 0; h < H; h++) xn[(size_t)t * H + h] = round_bf16(rt[h] * inv);
+  }
+}

@@ -105,6 +105,15 @@ void orc_unpack_int4(const uint8_t *p, size_t n, int8_t *q);
 void orc_pack_int2(const int8_t *q, size_t n, uint8_t *out);     /* n multiple of 4 */
 void orc_unpack_int2(const uint8_t *p, size_t n, int8_t *q);
 
+/* ---- a stack of layers ([DEEP] §4.3: a layer's merged output feeds the next layer) ----
+ * The pages leave the stacking arithmetic open.  Reading: the stack keeps a residual
+ * stream r [T][H]; after a layer, r <- r + out (out = the layer's MoE output), and the next
+ * layer's input is the unweighted RMSNorm of r, x = r / sqrt(mean_h(r^2) + eps), rounded to
+ * bf16 (the layers' activation type).  `add` may be NULL (the first layer: r = x_0).
+ * Writes r in place, xn [T][H] in fp64 (the rounded bf16 values, exactly). */
+void orc_residual_rmsnorm(int T, int H, double *r, const double *add, double eps,
+                          double *xn);
+
 #ifdef __cplusplus
 }
 #endif

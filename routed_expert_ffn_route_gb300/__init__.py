@@ -38,7 +38,7 @@ EXPORTED = [
     "moe_unpack_weights", "moe_route_topk", "moe_layer_forward", "moe_read_status",
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
     "moe_debug_wait_timeout", "moe_layer_forward_timed", "moe_forward_launches",
-    "moe_layer_forward_static",
+    "moe_layer_forward_static", "moe_residual_rmsnorm",
 ]
 
 # stages bracketed by the events of moe_layer_forward_timed
@@ -110,6 +110,7 @@ def _bind(L):
         "moe_layer_forward_timed": (I, [P, P, P, I, I, P, P, P, P, S, P, I, P]),
         "moe_forward_launches": (I, [P, I]),
         "moe_layer_forward_static": (I, [P, P, P, I, I, P, P, P, P, P]),
+        "moe_residual_rmsnorm": (I, [I, I, P, P, P, C.c_float, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -264,3 +265,12 @@ def moe_debug_block_dots(cfg, packed, expert, which, rows, qa, dots, stream=None
 def moe_debug_wait_timeout(ws, iterations, stream=None):
     _ck(lib().moe_debug_wait_timeout(_p(ws), ws.numel(), int(iterations), _stream(stream)),
         "moe_debug_wait_timeout")
+
+
+def moe_residual_rmsnorm(resid, add, x_next, x0=None, eps=1e-6, stream=None):
+    """Stack step: resid = x0 (bf16 [T,H]) if given, else resid += add (fp32 [T,H], in place;
+    add may be None); then x_next (bf16 [T,H]) = RMSNorm(resid) rounded to bf16."""
+    T, H = resid.shape
+    _ck(lib().moe_residual_rmsnorm(T, H, _p(resid), None if add is None else _p(add),
+                                   None if x0 is None else _p(x0), float(eps), _p(x_next),
+                                   _stream(stream)), "moe_residual_rmsnorm")

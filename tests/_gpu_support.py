@@ -82,3 +82,20 @@ def oracle_out(spec, L: GpuLayer, x, ids, w, tokens=None):
     sh = shared_expert(spec, L.seed, L.layer)
     return oracle.layer_experts(spec, x[tok].astype(np.float64), ids[tok], w[tok], experts, sh,
                                 mode=1)
+
+
+def make_experts_fast(spec, seed, layer, which) -> dict:
+    """As _support.make_experts, with the codes drawn by the generator's device variant
+    (the same counter-based stream, bit-identical to the host one; see test_gen) and copied
+    to the host: the GPU tests build many large experts for the oracle."""
+    from _support import make_expert  # noqa: F401 (same fields)
+    out = {}
+    for e in which:
+        e = int(e)
+        codes = {w: gen.expert_codes_torch(spec, seed, layer, e, w, "cuda").cpu().numpy()
+                 for w in ("gate", "up", "down")}
+        out[e] = oracle.Expert(gate=codes["gate"], up=codes["up"], down=codes["down"],
+                               s_gate=gen.expert_scales(spec, seed, layer, e, "gate"),
+                               s_up=gen.expert_scales(spec, seed, layer, e, "up"),
+                               s_down=gen.expert_scales(spec, seed, layer, e, "down"))
+    return out

@@ -1,0 +1,184 @@
+"""The stacked configuration: 8 DeepSeek-V3-shaped layers, router bias skewed Zipf(1.1),
+T = 4096 prefill and T = 1 decode steps (the stack step is the library's reading: residual
+stream + unweighted RMSNorm between layers).
+
+Parity is per layer: the oracle runs sampled tokens through its own fp64 stack, and at
+every layer the GPU layer runs on the oracle's bf16 input for those tokens (no oracle input
+comes from the GPU).  Expert ids are compared exactly where the oracle's decision margin is
+>= 1e-4 (the stack's deeper inputs cannot be redrawn), weights and outputs within the
+layer's tolerance wherever the routing matched.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+import routed_expert_ffn_route_gb300 as moe
+from routed_expert_ffn_route_gb300.stack import Stack
+from gen.device import build_packed_layer, hidden_to_device
+from _support import FROB_REL, MAX_REL_RMS, err_stats
+from _gpu_support import make_experts_fast
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LAYERS, SEED, T_PREFILL, EPS = 8, 0, 4096, 1e-6
+
+
+def zipf_beta():
+    for line in open(os.path.join(HERE, "golden", "zipf_beta.txt")):
+        if line.startswith("beta "):
+            return float(line.split()[1])
+    raise RuntimeError("zipf_beta.txt has no beta")
+
+
+SPEC = gen.spec("dsv3")
+
+
+def bias(layer):
+    return gen.zipf_bias(SPEC, SEED, layer, zipf_beta())
+
+
+@pytest.fixture(scope="module")
+def c5():
+    torch.cuda.empty_cache()
+    layers = [build_packed_layer(SPEC, SEED, l, "cuda", bias=bias(l)) for l in range(LAYERS)]
+    yield layers
+    del layers
+    torch.cuda.empty_cache()
+
+
+def bf16_bits(v64):
+    """fp64 values that are exactly bf16 numbers -> their bf16 bit patterns."""
+    b = np.ascontiguousarray(v64, dtype=np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0)
+    return (b >> 16).astype(np.uint16)
+
+
+def to_device_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+
+def test_stack_step_matches_oracle():
+    """moe_residual_rmsnorm against the oracle's stack step, on seeded inputs."""
+    rng = np.random.default_rng(11)
+    T, H = 7, SPEC.hidden
+    x0 = gen.bf16_round_bits((rng.standard_normal((T, H)) * 3).astype(np.float32))
+    x0f = x0.astype(np.uint32) << 16
+    x0_64 = x0f.view(np.float32).astype(np.float64)
+    add = rng.standard_normal((T, H)).astype(np.float32)
+    r_dev = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    x_dev = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    x0_dev = to_device_bf16(x0)
+    add_dev = torch.from_numpy(add).cuda()
+    # first step: r = x0, x = RMSNorm(r)
+    moe.moe_residual_rmsnorm(r_dev, None, x_dev, x0=x0_dev, eps=EPS)
+    r64, xn64 = oracle.residual_rmsnorm(x0_64, None, eps=EPS)
+    assert np.array_equal(r_dev.cpu().numpy().astype(np.float64), r64)
+    got = x_dev.view(torch.int16).cpu().numpy().view(np.uint16)
+    want = bf16_bits(xn64)
+    ulps = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert ulps.max() <= 1 and np.mean(ulps == 0) > 0.99
+    # next step: r += add (fp32 on the GPU, fp64 in the oracle)
+    moe.moe_residual_rmsnorm(r_dev, add_dev, x_dev, eps=EPS)
+    r64, xn64 = oracle.residual_rmsnorm(r64, add.astype(np.float64), eps=EPS)
+    r_got = r_dev.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(r_got - r64) <= 2.0 ** -23 * np.abs(r64) + 1e-30)
+    got = x_dev.view(torch.int16).cpu().numpy().view(np.uint16)
+    ulps = np.abs(got.astype(np.int32) - bf16_bits(xn64).astype(np.int32))
+    assert ulps.max() <= 1 and np.mean(ulps == 0) > 0.99
+
+
+def oracle_stack(x0_64):
+    """The oracle's own stack for a few tokens: per layer (input, ids, w, margin, out)."""
+    r, xn = oracle.residual_rmsnorm(x0_64, None, eps=EPS)
+    rec = []
+    for l in range(LAYERS):
+        wr = gen.router_weights(SPEC, SEED, l)
+        ids, w, margin = oracle.route(SPEC, oracle.router_logits(SPEC, xn, wr), bias(l))
+        need = sorted(set(int(e) for e in ids.ravel()))
+        experts = make_experts_fast(SPEC, SEED, l, need + [SPEC.n_experts])
+        sh = experts.pop(SPEC.n_experts)
+        out = oracle.layer_experts(SPEC, xn, ids, w, experts, sh, mode=1)
+        rec.append((xn, ids, w, margin, out))
+        r, xn = oracle.residual_rmsnorm(r, out, eps=EPS)
+    return rec
+
+
+def check_layers(layers, rec, rows, fill_bits, T):
+    """Run each GPU layer on a batch of T tokens whose `rows` hold the oracle's inputs."""
+    compared = 0
+    for l, (cfg, packed) in enumerate(layers):
+        xn, ids_o, w_o, margin, out_o = rec[l]
+        bits = fill_bits.copy()
+        bits[rows] = bf16_bits(xn)
+        x = to_device_bf16(bits)
+        out = torch.empty((T, SPEC.hidden), dtype=torch.float32, device="cuda")
+        ids = torch.empty((T, SPEC.top_k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, SPEC.top_k), dtype=torch.float32, device="cuda")
+        ws = torch.zeros(moe.moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+        moe.moe_layer_forward(cfg, packed, x, out, ids, w, ws)
+        assert moe.moe_read_status(ws) == moe.MOE_OK
+        ids_g = ids.cpu().numpy()[rows]
+        w_g = w.cpu().numpy()[rows]
+        out_g = out.cpu().numpy()[rows]
+        for i in range(len(rows)):
+            same = np.array_equal(ids_g[i], ids_o[i])
+            if margin[i] >= 1e-4:
+                assert same, f"layer {l} token {rows[i]}: ids {ids_g[i]} vs oracle {ids_o[i]}"
+            if same:
+                mx, fr = err_stats(out_g[i:i + 1], out_o[i:i + 1])
+                print(f"layer {l} row {rows[i]}: max|err|/RMS = {mx:.2e}, rel Frobenius = {fr:.2e}")
+                assert mx <= MAX_REL_RMS and fr <= FROB_REL
+                assert np.allclose(w_g[i], w_o[i], rtol=1e-5, atol=1e-7)
+                compared += 1
+    return compared
+
+
+def test_c5_prefill_and_decode_parity(c5):
+    """Per-layer parity of the T = 4096 prefill batch and of one T = 1 decode step."""
+    x, bits = gen.hidden_states(SPEC, SEED, 60, T_PREFILL)
+    rows = [0, T_PREFILL - 1]
+    rec = oracle_stack(x[rows].astype(np.float64))
+    n = check_layers(c5, rec, rows, bits, T_PREFILL)
+    xd, bd = gen.hidden_states(SPEC, SEED, 61, 1)  # a decode step: a fresh token
+    rec = oracle_stack(xd.astype(np.float64))
+    n += check_layers(c5, rec, [0], bd, 1)
+    assert n >= (len(rows) + 1) * LAYERS - 2  # at most two near-tie divergences skipped
+
+
+def test_c5_gpu_stack(c5):
+    """The whole stack on the GPU (prefill T = 4096, then decode steps of T = 1): status
+    clean, outputs finite, layer-0 routing equal to the oracle's where its margin allows,
+    and the Zipf skew visible in layer 0's selection frequencies."""
+    st = Stack(c5, T_PREFILL, eps=EPS)
+    x, bits = gen.hidden_states(SPEC, SEED, 60, T_PREFILL)
+    r = st.forward(hidden_to_device(SPEC, x, bits))
+    st.status()
+    assert torch.isfinite(r).all()
+    ids0 = st.ids[0][:T_PREFILL].cpu().numpy()
+    rows = [0, 1, 2, T_PREFILL - 1]
+    _, xn = oracle.residual_rmsnorm(x[rows].astype(np.float64), None, eps=EPS)
+    ids_o, _, margin = oracle.route(SPEC, oracle.router_logits(SPEC, xn, gen.router_weights(SPEC, SEED, 0)),
+                                    bias(0))
+    for i, t in enumerate(rows):
+        if margin[i] >= 1e-4:
+            assert np.array_equal(ids0[t], ids_o[i])
+    freq = np.bincount(ids0.ravel(), minlength=SPEC.n_experts) / T_PREFILL
+    rank = gen.zipf_rank(SPEC, SEED, 0)
+    by_rank = np.empty(SPEC.n_experts)
+    by_rank[rank - 1] = freq
+    r_ = np.arange(8, 129)
+    f = by_rank[7:128]
+    keep = f > 0
+    slope = np.polyfit(np.log(r_[keep]), np.log(f[keep]), 1)[0]
+    print(f"layer-0 selection slope over ranks 8..128: {slope:.3f}")
+    assert -1.6 < slope < -0.7
+    for step in range(4):
+        xd, bd = gen.hidden_states(SPEC, SEED, 1000 + step, 1)
+        r1 = st.forward(hidden_to_device(SPEC, xd, bd))
+        st.status()
+        assert torch.isfinite(r1).all()

@@ -45,6 +45,12 @@ MUTANTS = {
                     "acc += x[(size_t)t * H + h] * (double)wr[((size_t)h * E + e) % ((size_t)E * H)];"),
     "sigmoid_sign": ("double s = 1.0 / (1.0 + exp(-l[e]));", "double s = 1.0 / (1.0 + exp(l[e]));"),
     "block_dot_offset": ("acc += (int32_t)a[i] * (int32_t)b[i];", "acc += (int32_t)a[i] * (int32_t)b[31 - i];"),
+    "rmsnorm_sum_not_mean": ("const double inv = 1.0 / sqrt(ss / H + eps);",
+                             "const double inv = 1.0 / sqrt(ss + eps);"),
+    "rmsnorm_residual_dropped": ("if (add)\n      for (int h = 0; h < H; h++) rt[h] += add[(size_t)t * H + h];",
+                                 "if (0)\n      for (int h = 0; h < H; h++) rt[h] += add[(size_t)t * H + h];"),
+    "rmsnorm_not_rounded": ("xn[(size_t)t * H + h] = round_bf16(rt[h] * inv);",
+                            "xn[(size_t)t * H + h] = rt[h] * inv;"),
 }
 
 

@@ -481,3 +481,41 @@ def test_q8_layer_union_equals_per_token():
     a = oracle.layer_forward(s, x.astype(np.float64), wr, None, experts, None, mode=0)
     b = oracle.layer_forward(s, x.astype(np.float64), wr, None, experts, None, mode=1)
     assert all(np.array_equal(p, q) for p, q in zip(a, b))
+
+
+# ---------------------------------------------------------------- stack harness (residual + RMSNorm)
+
+def _bf16_exact(v):
+    """True where v (fp64) is exactly a bf16 number."""
+    f = v.astype(np.float32)
+    return (f.astype(np.float64) == v) & ((f.view(np.uint32) & 0xFFFF) == 0)
+
+
+def test_residual_rmsnorm_properties():
+    """RMSNorm output has unit RMS (up to the bf16 rounding of its elements), is exactly
+    invariant to scaling its input by a power of two (eps = 0), is bf16-representable, and
+    the residual update is the exact fp64 sum."""
+    rng = np.random.default_rng(7)
+    r0 = rng.standard_normal((5, 256)) * rng.uniform(0.1, 30.0, size=(5, 1))
+    add = rng.standard_normal((5, 256))
+    r1, x1 = oracle.residual_rmsnorm(r0, add, eps=0.0)
+    assert np.array_equal(r1, r0 + add)
+    rms = np.sqrt(np.mean(x1 * x1, axis=1))
+    assert np.all(np.abs(rms - 1.0) < 2.0 ** -8)
+    assert np.all(_bf16_exact(x1))
+    _, x2 = oracle.residual_rmsnorm(r1 * 8.0, None, eps=0.0)
+    assert np.array_equal(x1, x2)
+    # each element is the nearest bf16 of its exact normalised value: within half an ulp
+    exact = r1 / np.sqrt(np.mean(r1 * r1, axis=1, keepdims=True))
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(exact))) - 7)
+    assert np.all(np.abs(x1 - exact) <= 0.5 * ulp + 1e-300)
+
+
+def test_residual_rmsnorm_eps_and_first_layer():
+    """eps enters as mean(r^2) + eps (a constant row normalises to r/sqrt(r^2+eps)); with
+    no addend r is unchanged."""
+    r = np.full((1, 64), 0.01)
+    r1, x = oracle.residual_rmsnorm(r, None, eps=1e-4)
+    assert np.array_equal(r1, r)
+    want = 0.01 / np.sqrt(1e-4 + 1e-4)
+    assert np.all(np.abs(x - want) <= 2.0 ** -9 * abs(want))
