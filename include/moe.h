@@ -211,6 +211,16 @@ int moe_debug_block_dots(const moe_layer_config *cfg, const void *packed, int ex
                          const int32_t *rows, int n_rows, const int8_t *qa, int n_tok,
                          int32_t *dots, void *stream);
 
+/* Per-row weight quantiser ("colibrì 深度拆解" §5.1 quantize_row, per-row scaling): for each
+ * row r of w [rows][cols] (fp32 or bf16, device): amax = max |w|, scale[r] = amax / qmax
+ * (IEEE fp32 division), q = roundf(w / scale) (IEEE fp32 division, half away from zero)
+ * clamped to [-2^(bits-1), qmax], qmax = 2^(bits-1) - 1 (int4 as printed on the page; int8
+ * and int2 by the same pattern).  A zero row gives scale 0 and codes 0; a NaN ratio gives
+ * code 0.  q [rows][cols] int8 container and scale [rows] fp32 (device) are what
+ * moe_pack_weights / moe_pack_expert take.  bits: 8, 4 or 2. */
+int moe_quantize_rows(const void *w, moe_dtype dtype, int rows, int cols, int bits, int8_t *q,
+                      float *scale, void *stream);
+
 /* Debug: launch a one-block kernel whose bounded wait on a flag that nothing sets gives
  * up after `iterations` polls; it records MOE_ERR_TIMEOUT in the status word of `ws`
  * (read it with moe_read_status).  Exercises the timeout path without a fault. */

@@ -81,6 +81,7 @@ def _bind(lib):
     for f in ("orc_pack_int4", "orc_unpack_int4", "orc_pack_int2", "orc_unpack_int2"):
         getattr(lib, f).argtypes = [P, C.c_size_t, P]
     lib.orc_residual_rmsnorm.argtypes = [C.c_int, C.c_int, P, P, C.c_double, P]
+    lib.orc_quantize_rows.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
     return lib
 
 
@@ -260,3 +261,14 @@ def residual_rmsnorm(r: np.ndarray, add=None, eps: float = 1e-6):
     xn = np.empty_like(r)
     load().orc_residual_rmsnorm(T, H, _p(r), None if a is None else _p(a), float(eps), _p(xn))
     return r, xn
+
+
+def quantize_rows(w: np.ndarray, bits: int):
+    """Per-row quantiser: fp32 [rows, cols] -> (codes int8 [rows, cols], scales fp32 [rows])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, cols = w.shape
+    q = np.empty((rows, cols), dtype=np.int8)
+    s = np.empty(rows, dtype=np.float32)
+    if load().orc_quantize_rows(_p(w), rows, cols, int(bits), _p(q), _p(s)):
+        raise ValueError(f"unsupported bits {bits}")
+    return q, s

@@ -400,3 +400,30 @@ void orc_residual_rmsnorm(int T, int H, double *r, const double *add, double eps
     for (int h = 0; h < H; h++) xn[(size_t)t * H + h] = round_bf16(rt[h] * inv);
   }
 }
+
+int orc_quantize_rows(const float *w, int rows, int cols, int bits, int8_t *q, float *s) {
+  if (bits != 8 && bits != 4 && bits != 2) return -1;
+  const int qmax = (1 << (bits - 1)) - 1, qmin = -(1 << (bits - 1));
+  for (int r = 0; r < rows; r++) {
+    const float *row = w + (size_t)r * cols;
+    float amax = 0.0f;
+    for (int c = 0; c < cols; c++) {
+      const float a = fabsf(row[c]);
+      if (a > amax) amax = a;
+    }
+    volatile float sc = amax / (float)qmax; /* fp32, as the quantiser does it */
+    s[r] = sc;
+    for (int c = 0; c < cols; c++) {
+      int v = 0;
+      if (sc != 0.0f) {
+        volatile float ratio = row[c] / sc;
+        if (ratio == ratio) { /* a NaN ratio (inf / inf, NaN weights) gives code 0 */
+          const float rr = roundf(ratio);
+          v = rr < (float)qmin ? qmin : (rr > (float)qmax ? qmax : (int)rr);
+        }
+      }
+      q[(size_t)r * cols + c] = (int8_t)v;
+    }
+  }
+  return 0;
+}

@@ -105,6 +105,15 @@ void orc_unpack_int4(const uint8_t *p, size_t n, int8_t *q);
 void orc_pack_int2(const int8_t *q, size_t n, uint8_t *out);     /* n multiple of 4 */
 void orc_unpack_int2(const uint8_t *p, size_t n, int8_t *q);
 
+/* ---- quantiser ([DEEP] §5.1 quantize_row, per-row scaling) ----
+ * For each row r of w [rows][cols] (fp32): amax = max |w|, s = amax / qmax (fp32 IEEE
+ * division), q = roundf(w / s) (fp32 division, half away from zero) clamped to
+ * [-2^(bits-1), qmax], qmax = 2^(bits-1) - 1 (7 for int4 as printed; 127 and 1 for int8 and
+ * int2 by the same pattern); a row with amax == 0 gets s = 0 and q = 0, a NaN ratio gives
+ * q = 0 (non-finite weights are outside the pages' scheme).  Codes go to an
+ * int8 container [rows][cols], scales to s [rows].  bits: 8, 4 or 2. */
+int orc_quantize_rows(const float *w, int rows, int cols, int bits, int8_t *q, float *s);
+
 /* ---- a stack of layers ([DEEP] §4.3: a layer's merged output feeds the next layer) ----
  * The pages leave the stacking arithmetic open.  Reading: the stack keeps a residual
  * stream r [T][H]; after a layer, r <- r + out (out = the layer's MoE output), and the next

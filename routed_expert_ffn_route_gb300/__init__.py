@@ -38,7 +38,7 @@ EXPORTED = [
     "moe_unpack_weights", "moe_route_topk", "moe_layer_forward", "moe_read_status",
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
     "moe_debug_wait_timeout", "moe_layer_forward_timed", "moe_forward_launches",
-    "moe_layer_forward_static", "moe_residual_rmsnorm",
+    "moe_layer_forward_static", "moe_residual_rmsnorm", "moe_quantize_rows",
 ]
 
 # stages bracketed by the events of moe_layer_forward_timed
@@ -111,6 +111,7 @@ def _bind(L):
         "moe_forward_launches": (I, [P, I]),
         "moe_layer_forward_static": (I, [P, P, P, I, I, P, P, P, P, P]),
         "moe_residual_rmsnorm": (I, [I, I, P, P, P, C.c_float, P, P]),
+        "moe_quantize_rows": (I, [P, I, I, I, I, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -274,3 +275,10 @@ def moe_residual_rmsnorm(resid, add, x_next, x0=None, eps=1e-6, stream=None):
     _ck(lib().moe_residual_rmsnorm(T, H, _p(resid), None if add is None else _p(add),
                                    None if x0 is None else _p(x0), float(eps), _p(x_next),
                                    _stream(stream)), "moe_residual_rmsnorm")
+
+
+def moe_quantize_rows(w, bits, q, scale, stream=None):
+    """Per-row quantiser: w fp32/bf16 [rows, cols] -> q int8 [rows, cols], scale fp32 [rows]."""
+    rows, cols = w.shape
+    _ck(lib().moe_quantize_rows(_p(w), _dtype(w), rows, cols, int(bits), _p(q), _p(scale),
+                                _stream(stream)), "moe_quantize_rows")

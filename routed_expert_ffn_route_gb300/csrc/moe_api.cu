@@ -297,6 +297,15 @@ int moe_q8_0_quantize(const void *x, moe_dtype dtype, int T, int n, int8_t *q, f
   return launch_q8_quantize(x, dtype, T, n, q, d, (cudaStream_t)stream);
 }
 
+int moe_quantize_rows(const void *w, moe_dtype dtype, int rows, int cols, int bits, int8_t *q,
+                      float *scale, void *stream) {
+  if (rows < 0 || cols <= 0 || (bits != 8 && bits != 4 && bits != 2)) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_DT_F32 && dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!w || !q || !scale) return MOE_ERR_INVALID_ARG;
+  return launch_quantize_rows(w, dtype, rows, cols, bits, q, scale, (cudaStream_t)stream);
+}
+
 int moe_debug_block_dots(const moe_layer_config *cfg, const void *packed, int expert, int which,
                          const int32_t *rows, int n_rows, const int8_t *qa, int n_tok,
                          int32_t *dots, void *stream) {

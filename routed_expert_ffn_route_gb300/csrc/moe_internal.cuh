@@ -214,6 +214,8 @@ int launch_unpack_expert(const moe_layer_config &c, const ExpertLayout &L, const
                          int8_t *gate, int8_t *up, int8_t *down, float *sg, float *su, float *sd,
                          cudaStream_t st);
 int launch_write_header(const moe_layer_config &c, uint8_t *packed, cudaStream_t st);
+int launch_quantize_rows(const void *w, moe_dtype dt, int rows, int cols, int bits, int8_t *q,
+                         float *scale, cudaStream_t st);
 int launch_q8_quantize(const void *x, moe_dtype dt, int T, int n, int8_t *q, float *d,
                        cudaStream_t st);
 int launch_block_dots(const moe_layer_config &c, const uint8_t *mat, int K, int mat_rows,

@@ -212,6 +212,49 @@ int launch_q8_quantize(const void *x, moe_dtype dt, int T, int n, int8_t *q, flo
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------- per-row weight quantiser
+// "colibrì 深度拆解" §5.1 quantize_row, generalised by its own pattern: s = amax / qmax
+// (fp32 IEEE division), q = roundf(w / s) (fp32 IEEE division, half away from zero)
+// clamped to [-2^(bits-1), qmax]; amax == 0 gives s = 0 and q = 0; a NaN ratio gives 0.
+// One CTA per row.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const void *w, int is_bf16, int cols,
+                                                            int bits, int8_t *q, float *scale) {
+  const int r = blockIdx.x;
+  const size_t base = (size_t)r * cols;
+  auto at = [&](int c) {
+    return is_bf16 ? bf16_to_f32(((const uint16_t *)w)[base + c]) : ((const float *)w)[base + c];
+  };
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) amax = fmaxf(amax, fabsf(at(c)));
+  __shared__ float part[8];
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) amax = fmaxf(amax, part[i]);
+  const int qmax = (1 << (bits - 1)) - 1, qmin = -(1 << (bits - 1));
+  const float s = __fdiv_rn(amax, (float)qmax);
+  if (threadIdx.x == 0) scale[r] = s;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) {
+    int v = 0;
+    if (s != 0.f) {
+      const float ratio = __fdiv_rn(at(c), s);
+      if (ratio == ratio) {
+        const float rr = roundf(ratio);
+        v = rr < (float)qmin ? qmin : (rr > (float)qmax ? qmax : (int)rr);
+      }
+    }
+    q[base + c] = (int8_t)v;
+  }
+}
+
+int launch_quantize_rows(const void *w, moe_dtype dt, int rows, int cols, int bits, int8_t *q,
+                         float *scale, cudaStream_t st) {
+  quantize_rows_kernel<<<rows, 256, 0, st>>>(w, dt == MOE_DT_BF16, cols, bits, q, scale);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------- int8 block dots (debug)
 // dots[r][t][b] for matrix rows rows[r]; same device routine as the Q8_0 expert kernels.
 __global__ void block_dots_kernel(const uint8_t *mat, int K, int mat_rows, int which,

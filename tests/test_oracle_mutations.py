@@ -49,6 +49,10 @@ MUTANTS = {
                              "const double inv = 1.0 / sqrt(ss + eps);"),
     "rmsnorm_residual_dropped": ("if (add)\n      for (int h = 0; h < H; h++) rt[h] += add[(size_t)t * H + h];",
                                  "if (0)\n      for (int h = 0; h < H; h++) rt[h] += add[(size_t)t * H + h];"),
+    "quant_round_half_even": ("const float rr = roundf(ratio);", "const float rr = rintf(ratio);"),
+    "quant_scale_qmax_plus_1": ("volatile float sc = amax / (float)qmax;",
+                                "volatile float sc = amax / (float)(qmax + 1);"),
+    "quant_truncate": ("const float rr = roundf(ratio);", "const float rr = truncf(ratio);"),
     "rmsnorm_not_rounded": ("xn[(size_t)t * H + h] = round_bf16(rt[h] * inv);",
                             "xn[(size_t)t * H + h] = rt[h] * inv;"),
 }

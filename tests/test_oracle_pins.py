@@ -519,3 +519,40 @@ def test_residual_rmsnorm_eps_and_first_layer():
     assert np.array_equal(r1, r)
     want = 0.01 / np.sqrt(1e-4 + 1e-4)
     assert np.all(np.abs(x - want) <= 2.0 ** -9 * abs(want))
+
+
+# ---------------------------------------------------------------- quantiser ([DEEP] §5.1)
+
+def test_quantize_hand_worked():
+    """Rows whose scale is a power of two, so every ratio is exact: s = amax / qmax, codes
+    round half away from zero ("colibrì 深度拆解" §5.1 quantize_row, roundf)."""
+    # int4: amax 3.5 -> s = 0.5; ratios 7, -3.5, 0.5, 0, -7, 1.5 -> 7, -4, 1, 0, -7, 2
+    q, s = oracle.quantize_rows(np.array([[3.5, -1.75, 0.25, 0.0, -3.5, 0.75]], np.float32), 4)
+    assert s[0] == 0.5 and q.tolist() == [[7, -4, 1, 0, -7, 2]]
+    # int8: amax 127 -> s = 1; -63.5 -> -64, 0.5 -> 1, -0.5 -> -1
+    q, s = oracle.quantize_rows(np.array([[127.0, -63.5, 0.5, -0.5, 2.0, -127.0]], np.float32), 8)
+    assert s[0] == 1.0 and q.tolist() == [[127, -64, 1, -1, 2, -127]]
+    # int2: amax 1 -> s = 1; 0.5 -> 1, -0.5 -> -1, -1 -> -1, 0.25 -> 0
+    q, s = oracle.quantize_rows(np.array([[1.0, 0.5, -0.5, -1.0, 0.25, 0.0]], np.float32), 2)
+    assert s[0] == 1.0 and q.tolist() == [[1, 1, -1, -1, 0, 0]]
+    # a zero row: s = 0, codes 0
+    q, s = oracle.quantize_rows(np.zeros((1, 8), np.float32), 4)
+    assert s[0] == 0.0 and not q.any()
+
+
+@pytest.mark.parametrize("bits", [8, 4, 2])
+def test_quantize_properties(bits):
+    """Random rows: the largest magnitude maps to +-qmax, every code reconstructs its weight
+    to within half a step, codes stay in range, and scaling a row by 2 scales s by 2 with the
+    same codes (exact in fp32)."""
+    rng = np.random.default_rng(bits)
+    w = (rng.standard_normal((16, 96)) * rng.uniform(0.01, 5.0, (16, 1))).astype(np.float32)
+    q, s = oracle.quantize_rows(w, bits)
+    qmax = (1 << (bits - 1)) - 1
+    assert q.min() >= -(qmax + 1) and q.max() <= qmax
+    amax_col = np.argmax(np.abs(w), axis=1)
+    assert np.array_equal(np.abs(q[np.arange(16), amax_col]), np.full(16, qmax))
+    err = np.abs(w.astype(np.float64) - q.astype(np.float64) * s[:, None].astype(np.float64))
+    assert np.all(err <= 0.5 * s[:, None] * (1 + 1e-6))
+    q2, s2 = oracle.quantize_rows(w * 2, bits)
+    assert np.array_equal(q2, q) and np.array_equal(s2, 2 * s)
