@@ -58,6 +58,10 @@ def args_():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="profiling case instead of the benchmark: 'experts=E,T=T,forwards=N' "
+                         "runs N forwards of the DeepSeek-V3-shaped layer with E routed experts "
+                         "(L2 flushed before each) and prints one status line")
     ap.add_argument("--no-stack", action="store_true",
                     help="skip the 8-layer stack (prefill T=4096 + 256 decode steps)")
     ap.add_argument("--T", default=",".join(map(str, TS)),
@@ -585,8 +589,40 @@ def run_reference(a, rank, ws_n):
     }
 
 
+def run_case(spec_str):
+    """A small, self-contained workload for ncu captures (not a benchmark line)."""
+    import numpy as np
+    import torch
+
+    import gen
+    import routed_expert_ffn_route_gb300 as moe
+    from gen.device import build_packed_layer, hidden_to_device
+    kv = dict(p.split("=") for p in spec_str.split(","))
+    E, T, N = int(kv.get("experts", 32)), int(kv.get("T", 16)), int(kv.get("forwards", 3))
+    moe.lib()
+    torch.cuda.set_device(0)
+    s = gen.spec("dsv3").replace(n_experts=E)
+    cfg, packed = build_packed_layer(s, 0, 0, "cuda")
+    x, bits = gen.hidden_states(s, 1, 0, T)
+    xd = hidden_to_device(s, x, bits)
+    ws = torch.zeros(moe.moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, s.hidden), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, s.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, s.top_k), dtype=torch.float32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(N):
+        flush.zero_()
+        moe.moe_layer_forward(cfg, packed, xd, out, ids, w, ws)
+    st = moe.moe_read_status(ws)
+    print(f"case experts={E} T={T} forwards={N}: status {moe.moe_status_str(st)}, "
+          f"unique experts {np.unique(ids.cpu().numpy()).size}", flush=True)
+    return 0 if st == moe.MOE_OK else 1
+
+
 def main():
     a = args_()
+    if a.case:
+        sys.exit(run_case(a.case))
     rank, ws_n, local = dist_init(a.gpus)
     if a.impl == "reference":
         line = run_reference(a, rank, ws_n)
