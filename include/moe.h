@@ -182,9 +182,10 @@ int moe_layer_forward_static(const moe_layer_config *cfg, const void *packed, co
                              moe_dtype dtype, int T, float *out, int32_t *ids, float *w,
                              int32_t *status, void *stream);
 
-/* Number of kernel launches one moe_layer_forward makes for `cfg` and T tokens
- * (0 for T == 0; negative moe_status for an unsupported config). */
-int moe_forward_launches(const moe_layer_config *cfg, int T);
+/* Number of kernel launches one moe_layer_forward makes for `cfg`, hidden states of
+ * `dtype` and T tokens (0 for T == 0; negative moe_status for an unsupported config or
+ * dtype). */
+int moe_forward_launches(const moe_layer_config *cfg, moe_dtype dtype, int T);
 
 /* Synchronise `stream`, then return and clear the device status word of `ws`
  * (MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_NUMERIC, MOE_ERR_PACKED). */

@@ -108,7 +108,7 @@ def _bind(L):
         "moe_debug_block_dots": (I, [P, P, I, I, P, I, P, I, P, P]),
         "moe_debug_wait_timeout": (I, [P, S, I, P]),
         "moe_layer_forward_timed": (I, [P, P, P, I, I, P, P, P, P, S, P, I, P]),
-        "moe_forward_launches": (I, [P, I]),
+        "moe_forward_launches": (I, [P, I, I]),
         "moe_layer_forward_static": (I, [P, P, P, I, I, P, P, P, P, P]),
         "moe_residual_rmsnorm": (I, [I, I, P, P, P, C.c_float, P, P]),
         "moe_quantize_rows": (I, [P, I, I, I, I, P, P, P]),
@@ -238,8 +238,10 @@ def moe_layer_forward_static(cfg, packed, x, out, ids, w, status=None, stream=No
         "moe_layer_forward_static")
 
 
-def moe_forward_launches(cfg, T) -> int:
-    return lib().moe_forward_launches(C.byref(cfg), int(T))
+def moe_forward_launches(cfg, T, dtype=None) -> int:
+    """Kernel launches of one forward of T tokens (dtype: MOE_DT_BF16 by default)."""
+    d = MOE_DT_BF16 if dtype is None else int(dtype)
+    return lib().moe_forward_launches(C.byref(cfg), d, int(T))
 
 
 def moe_read_status(ws, stream=None) -> int:

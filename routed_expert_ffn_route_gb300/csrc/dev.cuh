@@ -52,6 +52,20 @@ __device__ __forceinline__ int dot32_s8(const uint32_t w[8], const int a[8]) {
   return acc;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while its predecessor in the stream is still running:
+// pdl_wait() blocks the calling thread until the predecessor grid has completed and its
+// memory is visible (a no-op without a programmatic predecessor), and pdl_trigger() lets
+// the successor grid start launching once every CTA of this grid has called it or exited.
+// Every kernel of the forward calls pdl_trigger() only after its own pdl_wait(), so when
+// a kernel starts, everything two launches back has completed; before its own pdl_wait()
+// a kernel reads only constant data (weights) or, through L2 (ld.global.cg), data of
+// kernels two or more launches back.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Poll *flag until it is >= want, at most `iterations` times (with a short sleep between
 // polls).  Returns false when the wait gave up; callers record MOE_ERR_TIMEOUT and return.
 __device__ __forceinline__ bool bounded_wait_ge(volatile int *flag, int want, long iterations) {

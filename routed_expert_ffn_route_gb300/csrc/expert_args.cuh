@@ -24,6 +24,9 @@ struct TcArgs {
   Ctrl *ctrl;
   int ns;
   const uint8_t *xg;  // gate/up B tiles (fp16, x_t * tscale[t])
+  const uint8_t *xt;    // decode-sized forwards: per-token fp16 rows [T][P][H] (register MMA)
+  const float *tscale;  // per token: the power-of-two activation scale
+  const int32_t *perm;  // slot of every permuted row (token = slot / k)
   float *rscale;      // per xg row: 1 / tscale of the row's token
   uint8_t *hg;        // gate/up output = down B tiles (fp16)
   float *y;           // down output [rows][H]
@@ -47,7 +50,9 @@ struct Item {
 
 template <bool DOWN>
 __device__ __forceinline__ bool tc_item(const TcArgs &a, int item, Item &it) {
-  const int n_groups = a.ctrl->n_groups;
+  // through L2: the down kernel's producer reads the work list before pdl_wait (it was
+  // written two launches back)
+  const int n_groups = __ldcg(&a.ctrl->n_groups);
   const int mt_s = DOWN ? a.H / 128 : a.LS.inter / 64;
   const int mt_r = DOWN ? a.H / 128 : a.LR.inter / 64;
   const int shi = a.ns * mt_s;
@@ -55,7 +60,11 @@ __device__ __forceinline__ bool tc_item(const TcArgs &a, int item, Item &it) {
   int gi;
   if (item < shi) { gi = item / mt_s; it.mt = item % mt_s; it.sh = true; }
   else { int i2 = item - shi; gi = a.ns + i2 / mt_r; it.mt = i2 % mt_r; it.sh = false; }
-  it.g = a.groups[gi];
+  {
+    const int4 *gp = (const int4 *)(a.groups + gi);
+    const int4 g0 = __ldcg(gp), g1 = __ldcg(gp + 1);
+    it.g = Group{g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  }
   const ExpertLayout &L = it.sh ? a.LS : a.LR;
   it.ebase = it.sh ? a.shared : a.routed + a.routed_stride * it.g.e;
   it.K = DOWN ? L.inter : a.H;
@@ -150,7 +159,6 @@ __device__ __forceinline__ void dq_word_i8(uint32_t w, uint32_t *o) {
 }
 
 // Small-group expert GEMMs (every group's B rows <= kMmaMaxRows): register-MMA kernel.
-constexpr int kMmaMaxRows = 16;
 int launch_experts_mma(int bits, bool down, TcArgs a, int rows_max, int kc_gcd, int bound,
                        int sms, cudaStream_t st);
 size_t mma_smem_bytes(int bits);

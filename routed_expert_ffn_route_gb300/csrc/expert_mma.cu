@@ -39,14 +39,17 @@ namespace moe {
 constexpr int kMmaWarps = 8;  // compute warps, 16 weight rows each
 constexpr int kMmaThreads = (kMmaWarps + 1) * 32;
 constexpr int kMmaRun = 4;               // chunks per run, where the item's K allows
-constexpr int kMmaBStage = kMmaRun * 16 * 128;  // 4 chunks x 16 activation rows x 128 B
+// activation stage: gate/up holds up to 16 token rows of a run (4 x 128 B, padded by 16 B
+// so that the fragment loads of 8 rows hit distinct banks); down holds the run's chunks of
+// the group's 128-byte-swizzled h tile (4 x 16 rows x 128 B)
+constexpr int kMmaBStage = 16 * (kMmaRun * 128 + 16);
 constexpr int kMmaMaxStages = 8;
 
-// ring geometry per code width: about 96 KB of stages, so two CTAs share an SM
+// ring geometry per code width: about 100 KB of stages, so two CTAs share an SM
 template <int BITS>
 struct MmaPlan {
   static constexpr int a_stage = kMmaRun * ATile<BITS>::bytes;
-  static constexpr int fit = (96 * 1024) / (a_stage + kMmaBStage);
+  static constexpr int fit = (100 * 1024) / (a_stage + kMmaBStage);
   static constexpr int stages = fit < kMmaMaxStages ? fit : kMmaMaxStages;
   static constexpr size_t smem = 1024 + (size_t)stages * (a_stage + kMmaBStage) + 256;
 };
@@ -89,6 +92,7 @@ template <int BITS, bool DOWN, int NT, int RA>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, int item_bound) {
   using PL = MmaPlan<BITS>;
   constexpr int S = PL::stages, AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
+  constexpr int RS = RA * 128 + 16;  // gate/up: bytes of one activation row in a stage
   extern __shared__ uint8_t smraw[];
   uint8_t *base = tc::align_smem_1024(smraw);
   uint8_t *bring = base;                   // S x kMmaBStage
@@ -113,41 +117,105 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
   };
 
   if (warp == kMmaWarps) {
-    // ------------------------------------------------ producer: codes + tiles, a copy per run
-    if (lane == 0) {
-      uint32_t armed = 0, last_ph = 0;
-      int run = 0;
-      bool ok = true;
+    // ------------------------------------------------ producer warp
+    uint32_t armed = 0, last_ph = 0;  // lane 0: stages with copies in flight, their phase
+    int run = 0;
+    bool ok = true;
+    if constexpr (DOWN) {
+      // Lane 0 copies each run of codes and the run's h tile.  The first S runs' code
+      // copies go out while the gate/up grid may still run; their h tiles (its output)
+      // only after pdl_wait.
+      bool waited = false;
+      const uint8_t *pend_src[S];
+      uint32_t pend_bytes[S];
+      auto release = [&](int n) {  // wait for the predecessor, then the deferred tiles
+        pdl_wait();
+        pdl_trigger();
+        if (lane == 0)
+          for (int q = 0; q < n; q++)
+            tc::bulk_g2s(bring + q * kMmaBStage, pend_src[q], pend_bytes[q], &bars->full[q]);
+        waited = true;
+      };
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
         if (!tc_item<DOWN>(a, item, it)) break;
         for (int kc = 0; kc < it.KC; kc += RA, run++) {
+          if (!waited && run == S) release(S);
           const int s = run % S;
           const uint32_t ph = (run / S) & 1;
-          if (!tc::mbar_wait(&bars->empty[s], ph ^ 1, abort, lim)) { ok = false; break; }
-          const uint32_t bbytes = (uint32_t)RA * it.rows8 * 128;
-          tc::mbar_arrive_expect_tx(&bars->full[s], RA * AB + bbytes);
-          tc::bulk_g2s(aring + s * PL::a_stage, a_src<BITS, DOWN>(a, it, kc), RA * AB,
-                       &bars->full[s]);
-          tc::bulk_g2s(bring + s * kMmaBStage, b_src<DOWN>(a, it, kc), bbytes, &bars->full[s]);
-          armed |= 1u << s;
-          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->empty[s], ph ^ 1, abort, lim));
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t bbytes = (uint32_t)RA * it.rows8 * 128;
+            tc::mbar_arrive_expect_tx(&bars->full[s], RA * AB + bbytes);
+            tc::bulk_g2s(aring + s * PL::a_stage, a_src<BITS, DOWN>(a, it, kc), RA * AB,
+                         &bars->full[s]);
+            if (waited) {
+              tc::bulk_g2s(bring + s * kMmaBStage, b_src<DOWN>(a, it, kc), bbytes,
+                           &bars->full[s]);
+            } else {  // run < S: stage s == run
+              pend_src[s] = b_src<DOWN>(a, it, kc);
+              pend_bytes[s] = bbytes;
+            }
+            armed |= 1u << s;
+            last_ph = (last_ph & ~(1u << s)) | (ph << s);
+          }
         }
       }
+      if (!waited) release(run < S ? run : S);
+    } else {
+      // Gate/up: lane 0 copies each run of codes, lane r the run's slice of group row r
+      // (its token's fp16 row, or row piece, written in front of this launch).
+      pdl_wait();
+      pdl_trigger();
+      Item it;
+      for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
+        if (!tc_item<DOWN>(a, item, it)) break;
+        const uint8_t *rsrc = nullptr;  // this lane's row
+        if (lane < it.rowsB) {
+          const int i = lane / a.P, piece = lane - i * a.P;
+          const int tok = it.sh ? it.g.pos0 + i : __ldcg(a.perm + it.g.pos0 + i) / a.k;
+          rsrc = a.xt + ((size_t)tok * a.P + piece) * a.H * 2;
+        }
+        for (int kc = 0; kc < it.KC; kc += RA, run++) {
+          const int s = run % S;
+          const uint32_t ph = (run / S) & 1;
+          ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->empty[s], ph ^ 1, abort, lim));
+          if (!ok) break;
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(&bars->full[s], RA * AB + (uint32_t)it.rowsB * RA * 128);
+            tc::bulk_g2s(aring + s * PL::a_stage, a_src<BITS, DOWN>(a, it, kc), RA * AB,
+                         &bars->full[s]);
+            armed |= 1u << s;
+            last_ph = (last_ph & ~(1u << s)) | (ph << s);
+          }
+          __syncwarp();  // the stage's byte count is set before its row copies start
+          if (lane < it.rowsB)
+            tc::bulk_g2s(bring + s * kMmaBStage + lane * RS, rsrc + (size_t)kc * 128, RA * 128,
+                         &bars->full[s]);
+        }
+      }
+    }
+    if (lane == 0) {
       if (!ok) give_up();
-      // every copy this thread started lands before the CTA exits (already true when the
+      // every copy this warp started lands before the CTA exits (already true when the
       // compute warps consumed them all)
       for (int q = 0; q < S; q++)
         if ((armed >> q) & 1) wait_nofail(&bars->full[q], (last_ph >> q) & 1, lim);
     }
   } else {
     // ------------------------------------------------ compute warp: weight rows 16w..16w+15
+    pdl_wait();
+    pdl_trigger();
     const int g = lane >> 2, t = lane & 3;
     const int r0 = 16 * warp + g, r1 = r0 + 8;  // the two rows of this lane's A fragments
     const int aoff0 = r0 * RB + (RB / 4) * t, aoff1 = aoff0 + 8 * RB;
     // activation row g of an 8-row tile: its 16-byte chunks 2t (k-steps 0, 1) and 2t+1
-    // (k-steps 2, 3), stored at chunk ^ (row & 7)
-    const int boff0 = g * 128 + (((2 * t) ^ g) << 4), boff1 = g * 128 + (((2 * t + 1) ^ g) << 4);
+    // (k-steps 2, 3); down tiles store chunk c of row r at c ^ (r & 7), gate/up rows are
+    // plain and RS bytes apart
+    const int boff0 = DOWN ? g * 128 + (((2 * t) ^ g) << 4) : g * RS + 32 * t;
+    const int boff1 = DOWN ? g * 128 + (((2 * t + 1) ^ g) << 4) : g * RS + 32 * t + 16;
+    constexpr int tile_step = DOWN ? 1024 : 8 * RS;  // bytes between 8-row tiles
     int run = 0;
     bool ok = true;
     Item it;
@@ -172,12 +240,12 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
           uint32_t q0[8], q1[8];  // rows r0 and r1: pairs 8t..8t+7
           dequant_quarter<BITS>(as + j * AB + aoff0, q0);
           dequant_quarter<BITS>(as + j * AB + aoff1, q1);
-          const uint8_t *bt = bs + j * bstride;
+          const uint8_t *bt = bs + (DOWN ? j * bstride : j * 128);
 #pragma unroll
           for (int n = 0; n < NT; n++) {
             if (n < nt) {
-              const uint4 c0 = *(const uint4 *)(bt + n * 1024 + boff0);
-              const uint4 c1 = *(const uint4 *)(bt + n * 1024 + boff1);
+              const uint4 c0 = *(const uint4 *)(bt + n * tile_step + boff0);
+              const uint4 c1 = *(const uint4 *)(bt + n * tile_step + boff1);
               const uint32_t a0[4] = {q0[0], q1[0], q0[1], q1[1]};
               const uint32_t a1[4] = {q0[2], q1[2], q0[3], q1[3]};
               const uint32_t a2[4] = {q0[4], q1[4], q0[5], q1[5]};
@@ -270,7 +338,8 @@ static int launch_mma(const TcArgs &a, int bound, int sms, cudaStream_t st) {
   constexpr size_t smem = MmaPlan<BITS>::smem;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int grid = 2 * sms < bound ? 2 * sms : bound;  // two CTAs per SM
-  k<<<grid, kMmaThreads, smem, st>>>(a, bound);
+  if (launch_pdl(k, dim3(grid), dim3(kMmaThreads), smem, st, a, bound) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -261,6 +261,8 @@ __global__ void __launch_bounds__(256) down_kernel(ExpertArgs a, int item_bound)
 // ---------------------------------------------------------------- combine
 __global__ void combine_kernel(int T, int H, int k, int n_shared, const float *w,
                                const int32_t *slot_pos, const float *y, float *out) {
+  pdl_wait();
+  pdl_trigger();
   long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   long per_t = H / 4;
   if (i >= (long)T * per_t) return;
@@ -353,8 +355,8 @@ static int run_gn(const moe_layer_config &c, const ExpertArgs &a, const WsLayout
 
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                   void *act, void *mid) {
-  if (W.tc) return launch_experts_tc(c, packed, x, dt, T, ws, W, st, act, mid);
+                   void *act, void *mid, bool front_rows) {
+  if (W.tc) return launch_experts_tc(c, packed, x, dt, T, ws, W, st, act, mid, front_rows);
   if (act && record_stage_event(act, st) != cudaSuccess) return MOE_ERR_CUDA;
   ExpertArgs a = make_args(c, packed, x, dt, T, ws, W);
   if (c.act_q8_0) return run_gn<8, true>(c, a, W, mid, st);
@@ -373,9 +375,10 @@ int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T
 int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st) {
   long n = (long)T * (c.hidden / 4);
-  combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(
-      T, c.hidden, c.top_k, c.n_shared, w, (const int32_t *)(ws + W.slot_pos),
-      (const float *)(ws + W.y), out);
+  if (launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, T, c.hidden,
+                 c.top_k, c.n_shared, w, (const int32_t *)(ws + W.slot_pos),
+                 (const float *)(ws + W.y), out) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

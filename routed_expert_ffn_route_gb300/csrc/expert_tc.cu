@@ -36,6 +36,7 @@
 
 #include "dev.cuh"
 #include "expert_args.cuh"
+#include "rows.cuh"
 #include "moe_internal.cuh"
 #include "tc.cuh"
 
@@ -221,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   __syncthreads();
   if (CL == 2) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::fence_after_sync();
+  pdl_wait();  // the set-up above overlaps the previous launch; the work list is its output
+  pdl_trigger();
   const uint32_t crank = CL == 2 ? tc::cluster_rank() : 0;
   const uint32_t tbase = bars->tmem_base;
   volatile int *abort = &bars->abort_flag;
@@ -507,6 +510,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
 // blockIdx.x: group; the warps of blockIdx.y stride over the group's rows.
 __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, int is_bf16,
                                                        const int32_t *perm, const float *tscale) {
+  pdl_wait();
+  pdl_trigger();
   const int gi = blockIdx.x;
   if (gi >= a.ctrl->n_groups) return;
   const Group g = a.groups[gi];
@@ -563,28 +568,50 @@ __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, 
   }
 }
 
+// Decode-sized forwards whose router did not write them: the per-token fp16 rows of the
+// register-MMA gate/up kernel (every block but the last) and every group row's 1 / scale
+// (the last block).
+__global__ void __launch_bounds__(256) token_rows_kernel(TcArgs a, const void *x, int is_bf16) {
+  pdl_wait();
+  pdl_trigger();
+  const int nb = gridDim.x - 1;
+  if ((int)blockIdx.x < nb) {
+    convert_token_rows(x, is_bf16, a.T, a.H, a.P, a.tscale, const_cast<uint8_t *>(a.xt),
+                       blockIdx.x * blockDim.x + threadIdx.x, nb * blockDim.x);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ng = a.ctrl->n_groups;
+  for (int gi = warp; gi < ng; gi += 8)
+    write_group_row_scales(a.groups[gi], a.E, a.k, a.P, a.perm, a.tscale, a.rscale, lane);
+}
+
 template <int BITS, bool DOWN, int NMAX>
 static int launch_tc(const TcArgs &a, int bound, int sms, bool pairs, cudaStream_t st) {
   constexpr size_t smem = tc_smem<NMAX, BITS>();
   if (!pairs) {
     auto k = tc_expert_kernel<BITS, DOWN, NMAX, 1>;
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    k<<<bound < sms ? bound : sms, kThreads, smem, st>>>(a, bound);
+    if (launch_pdl(k, dim3(bound < sms ? bound : sms), dim3(kThreads), smem, st, a, bound) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
   auto k = tc_expert_kernel<BITS, DOWN, NMAX, 2>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
   // as many clusters as can be resident at once (both CTAs of a cluster share a GPC)
   int clusters = 0;
   cfg.gridDim = dim3(2 * (sms / 2));
@@ -592,6 +619,7 @@ static int launch_tc(const TcArgs &a, int bound, int sms, bool pairs, cudaStream
     clusters = sms / 2;
   const int pairs_total = bound / 2;  // bound is even: every group has an even m-tile count
   cfg.gridDim = dim3(2 * std::min(clusters, pairs_total));
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, k, a, bound) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -616,26 +644,36 @@ static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
 template <int BITS>
 static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16,
                   const int32_t *perm, const float *tscale, cudaStream_t st, void *act,
-                  void *mid) {
+                  void *mid, bool front_rows) {
   DevInfo d = dev_info();
   if ((long)tc_smem<128, BITS>() > d.smem_optin || (long)tc_smem<32, BITS>() > d.smem_optin ||
       (long)mma_smem_bytes(BITS) > d.smem_optin)
     return MOE_ERR_UNSUPPORTED;
   // 8 warps per CTA, each with about eight 4-line steps of work; no more CTAs per group
   // than it takes to cover the SMs a few times over
-  const int rows8_max = round8(a.P * std::min(W.group_n, a.T));
-  const int gy = std::max(1, std::min((rows8_max * (a.H / kKChunk / 4) + 63) / 64,
-                                      (8 * d.sms + W.max_groups - 1) / W.max_groups));
-  gather_x_kernel<<<dim3(W.max_groups, gy), 256, 0, st>>>(a, x, is_bf16, perm, tscale);
+  // a group holds at most min(group_n, T) tokens (a token takes an expert at most once)
+  const int grows = W.group_n < a.T ? W.group_n : a.T;
+  // groups of at most 16 B rows (decode) take the register-MMA kernel, which reads
+  // per-token activation rows; larger ones the tensor-memory kernel and per-group tiles
+  const int rows_gu = a.P * grows;
+  if (rows_gu <= kMmaMaxRows) {
+    // about eight chunks of 8 elements per converting thread
+    const int nb = std::max(1, std::min(2 * d.sms, (a.T * (a.H / 8) + 2047) / 2048));
+    if (!front_rows && launch_pdl(token_rows_kernel, dim3(nb + 1), dim3(256), 0, st, a, x,
+                                  is_bf16) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    const int rows8_max = round8(a.P * std::min(W.group_n, a.T));
+    const int gy = std::max(1, std::min((rows8_max * (a.H / kKChunk / 4) + 63) / 64,
+                                        (8 * d.sms + W.max_groups - 1) / W.max_groups));
+    if (launch_pdl(gather_x_kernel, dim3(W.max_groups, gy), dim3(256), 0, st, a, x, is_bf16,
+                   perm, tscale) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (act && record_stage_event(act, st) != cudaSuccess) return MOE_ERR_CUDA;
   const int mt_s = a.LS.inter / 64, mt_r = a.LR.inter / 64, mt_d = a.H / 128;
   const int bound_gu = a.ns * mt_s + (W.max_groups - a.ns) * mt_r;
   const int bound_dn = W.max_groups * mt_d;
-  // a group holds at most min(group_n, T) tokens (a token takes an expert at most once)
-  const int grows = W.group_n < a.T ? W.group_n : a.T;
-  // groups of at most 16 B rows (decode) take the register-MMA kernel, larger ones the
-  // tensor-memory kernel
-  const int rows_gu = a.P * grows;
   int r = rows_gu <= kMmaMaxRows
               ? launch_experts_mma(BITS, false, a, rows_gu, a.H / kKChunk, bound_gu, d.sms, st)
               : launch_tc_n<BITS, false>(a, rows_gu, a.H / kKChunk, bound_gu, d.sms, st);
@@ -651,7 +689,7 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
 
 int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const void *x,
                       moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                      void *act, void *mid) {
+                      void *act, void *mid, bool front_rows) {
   PackLayout P = pack_layout(c);
   TcArgs a{};
   a.routed = packed + P.experts_off;
@@ -670,6 +708,8 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   a.ctrl = (Ctrl *)(ws + W.ctrl);
   a.ns = c.n_shared ? (T + W.group_n - 1) / W.group_n : 0;
   a.xg = ws + W.xg;
+  a.xt = ws + W.xg;  // decode-sized forwards use the region for token rows instead
+  a.tscale = (const float *)(ws + W.tscale);
   a.rscale = (float *)(ws + W.rscale);
   const float *tscale = (const float *)(ws + W.tscale);
   a.hg = ws + W.hg;
@@ -679,11 +719,12 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   a.trace = g_trace;
 #endif
   const int32_t *perm = (const int32_t *)(ws + W.perm);
+  a.perm = perm;
   const int is_bf16 = dt == MOE_DT_BF16;
   switch (c.weight_bits) {
-    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, act, mid);
-    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, act, mid);
-    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, act, mid);
+    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows);
+    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows);
+    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

@@ -223,16 +223,18 @@ static int forward_impl(const moe_layer_config *cfg, const void *packed, const v
   auto mark = [&](int i) {
     return ev ? record_stage_event(ev[i], st) == cudaSuccess : true;
   };
+  // decode-sized batches: selection, permutation and token rows in the router's launch
+  const bool fused = fused_front(*cfg, T, W.pieces);
   if (cudaMemsetAsync(ws, 0, sizeof(Ctrl), st) != cudaSuccess || !mark(0)) return MOE_ERR_CUDA;
-  if ((r = launch_router(*cfg, pk, x, dtype, T, ids, w, wsb, W, st))) return r;
+  if ((r = launch_router(*cfg, pk, x, dtype, T, ids, w, wsb, W, st, fused))) return r;
   if (!mark(1)) return MOE_ERR_CUDA;
-  if ((r = launch_permute(*cfg, T, ids, wsb, W, st))) return r;
+  if (!fused && (r = launch_permute(*cfg, T, ids, wsb, W, st))) return r;
   if (!mark(2)) return MOE_ERR_CUDA;
   if (cfg->act_q8_0 && (r = launch_quant_x(*cfg, x, dtype, T, wsb, W, st))) return r;
   // stage 2 ends when the activations are encoded: Q8_0 codes, or the tensor-core path's
-  // fp16 tiles (gathered inside launch_experts)
+  // fp16 tiles or token rows (written inside launch_experts unless the front wrote them)
   if ((r = launch_experts(*cfg, pk, x, dtype, T, wsb, W, st, ev ? ev[3] : nullptr,
-                          ev ? ev[4] : nullptr)))
+                          ev ? ev[4] : nullptr, fused)))
     return r;
   if (!mark(5)) return MOE_ERR_CUDA;
   if ((r = launch_combine(*cfg, T, w, out, wsb, W, st))) return r;
@@ -254,12 +256,16 @@ int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, con
   return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, events, stream);
 }
 
-int moe_forward_launches(const moe_layer_config *cfg, int T) {
+int moe_forward_launches(const moe_layer_config *cfg, moe_dtype dtype, int T) {
   int r = check(cfg);
   if (r) return r;
+  if (dtype != MOE_DT_F32 && dtype != MOE_DT_BF16) return MOE_ERR_INVALID_ARG;
   if (T <= 0) return 0;
-  // router logits + top-k, permute, [Q8_0 encode], [activation tile gather], gate/up,
-  // down, combine
+  const int pieces = dtype == MOE_DT_F32 ? 2 : 1;
+  // decode front (router, selection, permutation, token rows), gate/up, down, combine
+  if (fused_front(*cfg, T, pieces)) return 4;
+  // router logits + selection, permute, [Q8_0 encode], [activation tiles or token rows],
+  // gate/up, down, combine
   return 2 + 1 + (cfg->act_q8_0 ? 1 : 0) + (use_tc(*cfg) ? 1 : 0) + 2 + 1;
 }
 

@@ -93,12 +93,12 @@ struct Ctrl {
   int status;      // moe_status recorded on the device (0 = OK)
   int detail;      // where it was recorded (kernel id)
   int n_groups;    // groups written by the permute kernel (shared groups included)
-  int pad0;
-  int gemv_done[32];  // router GEMV: H-slice CTAs finished, per block of 8 experts
-  int pad[28];
+  int front_done;  // fused decode front: expert blocks of the router GEMV finished
+  int pad[60];
 };
 
 constexpr int kRouterHS = 8;   // H splits of the small-T router GEMV
+constexpr int kMmaMaxRows = 16;  // largest group (activation rows) of the register-MMA kernels
 constexpr int kTcMaxRows = 128;  // B-operand rows (tokens x pieces) of one tensor-core group
 
 // Expert kernels: tcgen05 tensor-core GEMMs for float activations; the CUDA-core dp4a
@@ -153,6 +153,22 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   return W;
 }
 
+// The router takes the GEMV path (logits split over H slices) for small batches.
+static inline bool router_gemv(const moe_layer_config &c, int T) {
+  return T <= 16 && (size_t)T * (c.hidden / kRouterHS) * 4 <= 96 * 1024;
+}
+
+// Decode-sized forwards: every gate/up group fits the register-MMA kernel (pieces x tokens
+// <= 16 rows).  Those kernels read each token's fp16 activation row (xt, at the start of
+// the xg region) instead of per-group tiles; with the GEMV router, the GEMV's last CTA
+// also selects, permutes and writes those rows (one launch in front of the expert GEMMs).
+static inline bool decode_rows(const moe_layer_config &c, int T, int pieces) {
+  return use_tc(c) && T <= kTcMaxRows / pieces && pieces * T <= kMmaMaxRows;
+}
+static inline bool fused_front(const moe_layer_config &c, int T, int pieces) {
+  return decode_rows(c, T, pieces) && router_gemv(c, T);
+}
+
 // ---------------------------------------------------------------- device helpers
 enum KernelId { kKRouter = 1, kKTopk = 2, kKPermute = 3, kKGateUp = 4, kKDown = 5,
                 kKCombine = 6, kKQuant = 7, kKDebugWait = 8 };
@@ -183,6 +199,24 @@ static inline cudaError_t record_stage_event(void *ev, cudaStream_t st) {
              : cudaEventRecord((cudaEvent_t)ev, st);
 }
 
+// Launch `k` on `st` with programmatic stream serialisation: the kernel may begin while
+// its predecessor finishes, and calls pdl_wait() before it touches the predecessor's output.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 struct DevInfo {
   int sms;
   int smem_optin;
@@ -190,21 +224,23 @@ struct DevInfo {
 DevInfo dev_info();
 
 // kernels (one translation unit each)
+// fused: the decode front (selection, permutation and activation rows in the GEMV launch)
 int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *x, moe_dtype dt,
                   int T, int32_t *ids, float *w, uint8_t *ws, const WsLayout &W,
-                  cudaStream_t st);
+                  cudaStream_t st, bool fused = false);
 int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
 int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
 int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const void *x,
                       moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                      void *act, void *mid);
+                      void *act, void *mid, bool front_rows);
 // act_event / mid_event (cudaEvent_t or null) are recorded after the activation encoding
-// (tensor-core path: the fp16 tile gather) and between the gate/up and down launches
+// (tensor-core path: the fp16 tile gather or token rows) and between the gate/up and down
+// launches; front_rows: the fused decode front already wrote the token rows
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
-                   void *act_event, void *mid_event);
+                   void *act_event, void *mid_event, bool front_rows = false);
 int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
                    const WsLayout &W, cudaStream_t st);
 int launch_pack_expert(const moe_layer_config &c, const ExpertLayout &L, const int8_t *gate,

@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
                                                        int32_t *slot_pos, Group *groups,
                                                        Ctrl *ctrl) {
   extern __shared__ uint32_t sm[];
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_chunks = (T + 31) / 32;
   uint32_t *masks = sm;                                    // [32][E]
@@ -140,10 +142,11 @@ int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t
   if ((long)smem > d.smem_optin) return MOE_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  permute_kernel<<<1, 1024, smem, st>>>(
-      T, c.top_k, c.n_experts, c.n_shared, W.group_n, W.pieces, ids, (int32_t *)(ws + W.offsets),
-      (int32_t *)(ws + W.perm), (int32_t *)(ws + W.slot_pos), (Group *)(ws + W.groups),
-      (Ctrl *)(ws + W.ctrl));
+  if (launch_pdl(permute_kernel, dim3(1), dim3(1024), smem, st, T, c.top_k, c.n_experts,
+                 c.n_shared, W.group_n, W.pieces, ids, (int32_t *)(ws + W.offsets),
+                 (int32_t *)(ws + W.perm), (int32_t *)(ws + W.slot_pos), (Group *)(ws + W.groups),
+                 (Ctrl *)(ws + W.ctrl)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -135,3 +135,23 @@ def test_workspace_grows_with_tokens(L):
     a, b = moe.moe_workspace_bytes(cfg, 16), moe.moe_workspace_bytes(cfg, 2048)
     assert 0 < a < b
     assert b >= 2048 * 9 * 6144 * 4  # the fp32 expert outputs of every (token, slot)
+
+
+def test_forward_launch_counts(L):
+    """Decode-sized batches run as one front launch (router, selection, permutation,
+    token rows) plus gate/up, down and combine; other batches take the separate launches."""
+    dsv3 = config_for(gen.spec("dsv3"))
+    f32, bf16 = moe.MOE_DT_F32, moe.MOE_DT_BF16
+    assert moe.moe_forward_launches(dsv3, 0) == 0
+    assert moe.moe_forward_launches(dsv3, 1) == 4
+    assert moe.moe_forward_launches(dsv3, 16, bf16) == 4
+    assert moe.moe_forward_launches(dsv3, 8, f32) == 4      # two fp16 pieces per token
+    assert moe.moe_forward_launches(dsv3, 16, f32) == 7     # 32 rows: activation tiles
+    assert moe.moe_forward_launches(dsv3, 17, bf16) == 7
+    assert moe.moe_forward_launches(dsv3, 2048, bf16) == 7
+    # a hidden size whose T = 16 router slice does not fit the GEMV: separate launches
+    wide = config_for(gen.spec("tiny").replace(hidden=12416))
+    assert moe.moe_forward_launches(wide, 16, bf16) == 7
+    q8 = config_for(gen.spec("dsv3_int8"))
+    assert moe.moe_forward_launches(q8, 4, bf16) == 7      # Q8_0 encode, no tiles
+    assert L.moe_forward_launches(C.byref(dsv3), 7, 1) == moe.MOE_ERR_INVALID_ARG

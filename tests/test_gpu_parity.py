@@ -145,6 +145,19 @@ def test_layer_small_softmax_fp32():
     check_layer(small("softmax", x_dtype="f32"), 21, seed=7)
 
 
+@pytest.mark.parametrize("T", [5, 16])
+def test_layer_small_grouped_fp32(T):
+    # T = 5: the decode front with two fp16 pieces per token; T = 16: 32 activation rows,
+    # so gate/up takes the tile path while down stays on the register-MMA kernel
+    check_layer(small("grouped", x_dtype="f32"), T, seed=8)
+
+
+def test_layer_decode_rows_without_gemv_router():
+    # a hidden size whose router slices do not fit the GEMV at T = 16: the tiled router,
+    # selection, permute and token-row launches feed the register-MMA kernels
+    check_layer(small("softmax", hidden=12416, inter=256), 16, seed=9)
+
+
 def test_layer_deterministic_and_T0_noop():
     s = small("grouped")
     L = get_layer(s, 1)
