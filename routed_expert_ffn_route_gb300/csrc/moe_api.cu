@@ -123,7 +123,9 @@ int moe_pack_router(const moe_layer_config *cfg, const float *router_w, const fl
   cudaError_t e = router_bias
       ? cudaMemcpyAsync(base + P.router_b_off, router_bias, bbytes, cudaMemcpyDeviceToDevice, st)
       : cudaMemsetAsync(base + P.router_b_off, 0, bbytes, st);
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_router_tiles(*cfg, (const float *)(base + P.router_w_off),
+                             base + P.router_t_off, st);
 }
 
 int moe_pack_expert(const moe_layer_config *cfg, int expert, const int8_t *gate, const int8_t *up,

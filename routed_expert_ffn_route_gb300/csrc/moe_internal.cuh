@@ -1,7 +1,12 @@
 // moe_internal.cuh -- private layouts and helpers of the GB300 MoE-layer library.
 //
 // Packed weight blob (device memory, caller-owned; private layout, versioned header):
-//   [header 256 B][router_w fp32 E*H][router_bias fp32 E][expert 0]...[expert E-1][shared]
+//   [header 256 B][router_w fp32 E*H][router_bias fp32 E][router tiles]
+//   [expert 0]...[expert E-1][shared]
+// Router tiles: the fp32 router matrix as three bf16 pieces (w = hi + mid + lo exactly),
+// the tensor-core router's A operand: [piece][E/128 m-tiles][H/64 k-chunks] blocks of
+// [128 rows][64 bf16], 128-byte swizzled (16-byte chunk c of row r at c ^ (r & 7)); rows
+// past E are zero.
 // Every expert block is 4096-byte aligned and holds
 //   gate/up codes : (I/64 m-tiles) x (H/64 k-chunks) blocks of [128 rows][CB bytes]
 //                   rows interleaved: row 2j = gate row (64*mt + j), row 2j+1 = up row
@@ -27,7 +32,7 @@
 namespace moe {
 
 constexpr uint32_t kMagic = 0x50454F4Du;  // "MOEP"
-constexpr uint32_t kVersion = 1;
+constexpr uint32_t kVersion = 2;
 constexpr int kHeaderBytes = 256;
 constexpr int kKChunk = 64;     // contraction elements per chunk
 constexpr int kTileRows = 128;  // weight rows per block
@@ -45,9 +50,12 @@ struct ExpertLayout {
 };
 
 struct PackLayout {
-  uint64_t router_w_off, router_b_off, experts_off, shared_off, total;
+  uint64_t router_w_off, router_b_off, router_t_off, experts_off, shared_off, total;
   ExpertLayout routed, shared;
 };
+
+constexpr int kRouterTileBytes = 128 * 64 * 2;  // one router tile: 128 rows x 64 bf16
+static inline int router_mtiles(const moe_layer_config &c) { return (c.n_experts + 127) / 128; }
 
 static inline uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
 
@@ -70,7 +78,10 @@ static inline PackLayout pack_layout(const moe_layer_config &c) {
   int Is = c.inter_shared ? c.inter_shared : c.inter;
   P.router_w_off = kHeaderBytes;
   P.router_b_off = align_up(P.router_w_off + (uint64_t)c.n_experts * c.hidden * 4, 256);
-  P.experts_off = align_up(P.router_b_off + (uint64_t)c.n_experts * 4, 4096);
+  P.router_t_off = align_up(P.router_b_off + (uint64_t)c.n_experts * 4, 1024);
+  P.experts_off = align_up(P.router_t_off + (uint64_t)3 * router_mtiles(c) * (c.hidden / 64) *
+                                                kRouterTileBytes,
+                           4096);
   P.routed = expert_layout(c.hidden, c.inter, c.weight_bits);
   P.shared = expert_layout(c.hidden, Is, c.weight_bits);
   P.shared_off = P.experts_off + P.routed.bytes * (uint64_t)c.n_experts;
@@ -177,6 +188,17 @@ __device__ __forceinline__ void record_status(Ctrl *ctrl, int status, int where)
   if (atomicCAS(&ctrl->status, 0, status) == 0) ctrl->detail = where;
 }
 
+// The packed blob's header against the layer config (checked once per router launch).
+__device__ __forceinline__ void check_header(const uint8_t *packed, const moe_layer_config &c,
+                                             Ctrl *ctrl) {
+  const PackHeader *h = (const PackHeader *)packed;
+  int Is = c.inter_shared ? c.inter_shared : c.inter;
+  if (h->magic != kMagic || h->version != kVersion || h->hidden != c.hidden ||
+      h->inter != c.inter || h->inter_shared != Is || h->n_experts != c.n_experts ||
+      h->n_shared != c.n_shared || h->weight_bits != c.weight_bits)
+    record_status(ctrl, MOE_ERR_PACKED, kKRouter);
+}
+
 // A group: `n` permuted rows starting at `pos0` that all use expert `e`.  For the shared
 // expert (e == E), rows are tokens pos0 .. pos0+n-1.  xrow0 / hrow0: the group's first
 // row in the xg / hg tile buffers (tensor-core path).
@@ -250,6 +272,13 @@ int launch_unpack_expert(const moe_layer_config &c, const ExpertLayout &L, const
                          int8_t *gate, int8_t *up, int8_t *down, float *sg, float *su, float *sd,
                          cudaStream_t st);
 int launch_write_header(const moe_layer_config &c, uint8_t *packed, cudaStream_t st);
+int launch_router_tiles(const moe_layer_config &c, const float *router_w, uint8_t *tiles,
+                        cudaStream_t st);
+// router logits of large bf16 batches on the tensor cores: partials[hs][t][e] for hsplits
+// H slices (the selection adds them in slice order); false when the launch does not apply
+bool router_tc_applies(const moe_layer_config &c, moe_dtype dt, int T);
+int launch_router_tc(const moe_layer_config &c, const uint8_t *packed, const void *x, int T,
+                     float *partials, int hsplits, Ctrl *ctrl, cudaStream_t st);
 int launch_quantize_rows(const void *w, moe_dtype dt, int rows, int cols, int bits, int8_t *q,
                          float *scale, cudaStream_t st);
 int launch_q8_quantize(const void *x, moe_dtype dt, int T, int n, int8_t *q, float *d,

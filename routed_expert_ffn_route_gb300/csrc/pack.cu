@@ -7,6 +7,8 @@
 // 深度拆解", §5.1 量化).  The in-word order of the codes is this library's own: it is chosen
 // so that one shift-and-mask yields two adjacent contraction elements (see moe_internal.cuh).
 #include "moe_internal.cuh"
+#include <cuda_bf16.h>
+
 #include "dev.cuh"
 
 namespace moe {
@@ -165,6 +167,46 @@ int launch_unpack_expert(const moe_layer_config &c, const ExpertLayout &L, const
   scales_kernel<true><<<(n + 255) / 256, 256, 0, st>>>(
       c.hidden, L.inter, nullptr, nullptr, nullptr, sg, su, sd, (float *)(b + L.sgu_off),
       (float *)(b + L.sd_off));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// The router matrix as three bf16 pieces in tensor-core tiles: hi = bf16(w),
+// mid = bf16(w - hi), lo = bf16(w - hi - mid); each difference is exact in fp32 and lo
+// holds the last 8 of the 24 significant bits, so hi + mid + lo == w exactly.  A thread
+// writes one 16-byte chunk (8 elements) of one row of one piece's tile.
+__global__ void router_tiles_kernel(int E, int H, int MT, const float *w, uint8_t *tiles) {
+  const int KC = H / 64;
+  const long n = 3L * MT * KC * 128 * 8;
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int c = (int)(i & 7), r = (int)((i >> 3) & 127);
+  long q = i >> 10;
+  const int kc = (int)(q % KC);
+  q /= KC;
+  const int mt = (int)(q % MT), piece = (int)(q / MT);
+  const int e = mt * 128 + r;
+  uint16_t out[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) {
+    const float v = e < E ? w[(long)e * H + kc * 64 + c * 8 + j] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+    const __nv_bfloat16 pv = piece == 0 ? hi : (piece == 1 ? mid : lo);
+    out[j] = *(const uint16_t *)&pv;
+  }
+  uint8_t *dst = tiles + (((long)piece * MT + mt) * KC + kc) * kRouterTileBytes + r * 128 +
+                 ((c ^ (r & 7)) << 4);
+  *(uint4 *)dst = *(const uint4 *)out;
+}
+
+int launch_router_tiles(const moe_layer_config &c, const float *router_w, uint8_t *tiles,
+                        cudaStream_t st) {
+  const int MT = router_mtiles(c);
+  const long n = 3L * MT * (c.hidden / 64) * 128 * 8;
+  router_tiles_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(c.n_experts, c.hidden, MT,
+                                                                  router_w, tiles);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -50,15 +50,6 @@ extern long long *g_router_trace;
   } while (0)
 #endif
 
-__device__ __forceinline__ void check_header(const uint8_t *packed, const moe_layer_config &c,
-                                             Ctrl *ctrl) {
-  const PackHeader *h = (const PackHeader *)packed;
-  int Is = c.inter_shared ? c.inter_shared : c.inter;
-  if (h->magic != kMagic || h->version != kVersion || h->hidden != c.hidden ||
-      h->inter != c.inter || h->inter_shared != Is || h->n_experts != c.n_experts ||
-      h->n_shared != c.n_shared || h->weight_bits != c.weight_bits)
-    record_status(ctrl, MOE_ERR_PACKED, kKRouter);
-}
 
 // Router GEMV CTAs: a warp per expert row slice; the fused front's tail selects a token
 // per warp, so 16 warps take a batch of up to 16 tokens in one round.
@@ -783,6 +774,14 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
     else if (T <= 8) launch(router_gemv_kernel<8>);
     else launch(router_gemv_kernel<16>);
     if (fused) return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  } else if (router_tc_applies(c, dt, T)) {
+    // tensor cores: 128 experts x 256 tokens a CTA, H split until the grid covers the SMs
+    const int tiles = router_mtiles(c) * ((T + 255) / 256), KC = c.hidden / 64;
+    const int sms = dev_info().sms;
+    hsplits = 1;
+    while (hsplits < kRouterHS && tiles * hsplits < sms && KC % (2 * hsplits) == 0) hsplits *= 2;
+    const int r = launch_router_tc(c, packed, x, T, partials, hsplits, ctrl, st);
+    if (r) return r;
   } else {
     // 128 x 128 tiles for large T, 64 x 64 below; H split (partial sums added in order by
     // the selection kernel) until the grid covers the SMs twice

@@ -53,7 +53,8 @@ def test_packed_bytes_match_the_per_expert_sizes(L):
     s = gen.spec("dsv3")
     nb = moe.moe_packed_bytes(config_for(s))
     per_expert = (2 * 2048 * 6144 + 6144 * 2048) // 2 + (2 * 2048 + 6144) * 4  # 18.92 MB
-    router = 256 * 6144 * 4 + 256 * 4
+    # fp32 router matrix and bias, plus its three bf16 pieces in 128-row tensor-core tiles
+    router = 256 * 6144 * 4 + 256 * 4 + 3 * 2 * (6144 // 64) * 128 * 64 * 2
     assert per_expert == 18915328
     assert 257 * per_expert + router <= nb <= 257 * (per_expert + 8192) + router + 8192
     s8 = gen.spec("dsv3_int8")
