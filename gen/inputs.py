@@ -65,6 +65,7 @@ class LayerSpec:
     act_q8_0: int = 0      # 1: Q8_0 int8 activations (needs weight_bits == 8)
     x_dtype: str = "bf16"  # "f32" or "bf16"
     bias_std: float = 0.0  # router bias N(0, bias_std); 0 = no bias
+    top_p: float = 0.0     # adaptive expert top-p (0 = off; lossy, opt-in)
 
     @property
     def inter_sh(self) -> int:

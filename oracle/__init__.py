@@ -44,7 +44,8 @@ class _Cfg(C.Structure):
     _fields_ = [("hidden", C.c_int), ("inter", C.c_int), ("n_experts", C.c_int),
                 ("top_k", C.c_int), ("n_shared", C.c_int), ("inter_shared", C.c_int),
                 ("router", C.c_int), ("n_group", C.c_int), ("topk_group", C.c_int),
-                ("norm_topk", C.c_int), ("rsf", C.c_double), ("act_q8_0", C.c_int)]
+                ("norm_topk", C.c_int), ("rsf", C.c_double), ("act_q8_0", C.c_int),
+                ("top_p", C.c_double)]
 
 
 class _Expert(C.Structure):
@@ -94,7 +95,8 @@ def config(spec) -> _Cfg:
     """Oracle config from a gen.LayerSpec."""
     return _Cfg(spec.hidden, spec.inter, spec.n_experts, spec.top_k, spec.n_shared,
                 spec.inter_sh, 0 if spec.router == "softmax" else 1, spec.n_group,
-                spec.topk_group, spec.norm_topk, float(spec.rsf), spec.act_q8_0)
+                spec.topk_group, spec.norm_topk, float(spec.rsf), spec.act_q8_0,
+                float(spec.top_p))
 
 
 @dataclasses.dataclass

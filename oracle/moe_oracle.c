@@ -149,7 +149,33 @@ static int route_one(const orc_config *c, const double *l, const float *bias, in
   if (eg < mg) mg = eg;
   double wsum = 0.0;
   for (int j = 0; j < k; j++) { ids[j] = sorted[j]; wsum += wsrc[sorted[j]]; }
+  /* Adaptive expert top-p ("Show HN" 实用调节项 --topp, an explicit lossy override; the
+   * pages give no formula, reading): in slot order keep the shortest prefix of the
+   * selected experts whose share of the selection's weight sources reaches top_p (at
+   * least the first); the rest are dropped and the kept weights normalised over the kept
+   * experts.  Its decisions are "share before slot j < top_p"; the gaps at the crossing
+   * enter the margin. */
+  int m = k;
+  if (c->top_p > 0.0 && c->top_p < 1.0) {
+    double before = 0.0, before_last = 0.0;
+    m = 0;
+    for (int j = 0; j < k; j++) {
+      if (before >= c->top_p) break;
+      before_last = before;
+      before += wsrc[sorted[j]] / wsum;
+      m = j + 1;
+    }
+    double g1 = c->top_p - before_last;  /* the last kept slot */
+    if (g1 < mg) mg = g1;
+    if (m < k) {
+      double g2 = before - c->top_p;     /* the first dropped slot */
+      if (g2 < mg) mg = g2;
+    }
+    wsum = 0.0;
+    for (int j = 0; j < m; j++) wsum += wsrc[sorted[j]];
+  }
   for (int j = 0; j < k; j++) {
+    if (j >= m) { ids[j] = -1; w[j] = 0.0; continue; }
     double v = wsrc[sorted[j]];
     if (c->norm_topk) v = v / wsum;
     w[j] = v * c->rsf;
@@ -179,13 +205,15 @@ int orc_route(const orc_config *c, const double *logits, const float *bias, int 
 /* [README] 批处理并集 MoE: group the (token, slot) pairs by expert. */
 void orc_permutation(int T, int k, int E, const int32_t *ids, int32_t *offsets, int32_t *perm) {
   for (int e = 0; e <= E; e++) offsets[e] = 0;
-  for (int i = 0; i < T * k; i++) offsets[ids[i] + 1]++;
+  for (int i = 0; i < T * k; i++)
+    if (ids[i] >= 0) offsets[ids[i] + 1]++;
   for (int e = 0; e < E; e++) offsets[e + 1] += offsets[e];
   int pos = 0;
   for (int e = 0; e < E; e++)
     for (int t = 0; t < T; t++)
       for (int j = 0; j < k; j++)
         if (ids[t * k + j] == e) perm[pos++] = t * k + j;
+  while (pos < T * k) perm[pos++] = -1;
 }
 
 /* y[n][rows] = W x with W[r][c] = s[r] * q[r][c] (plain fp64) */
@@ -293,6 +321,7 @@ int orc_layer_experts(const orc_config *c, const double *x, int T, const int32_t
       if (c->n_shared) orc_expert_forward(c, shared, x + (size_t)t * H, 1, o);
       else for (int h = 0; h < H; h++) o[h] = 0.0;
       for (int j = 0; j < k; j++) {
+        if (ids[t * k + j] < 0) continue;  /* dropped by top-p */
         const orc_expert *ex = &experts[ids[t * k + j]];
         if (!ex->gate) { free(y); return -2; }
         orc_expert_forward(c, ex, x + (size_t)t * H, 1, y);
@@ -326,9 +355,11 @@ int orc_layer_experts(const orc_config *c, const double *x, int T, const int32_t
   if (c->n_shared) orc_expert_forward(c, shared, x, T, out);
   else for (size_t i = 0; i < (size_t)T * H; i++) out[i] = 0.0;
   for (int t = 0; t < T; t++)
-    for (int j = 0; j < k; j++)
+    for (int j = 0; j < k; j++) {
+      if (ids[t * k + j] < 0) continue;  /* dropped by top-p */
       for (int h = 0; h < H; h++)
         out[(size_t)t * H + h] += w[t * k + j] * yslot[((size_t)t * k + j) * H + h];
+    }
   free(offsets); free(perm); free(yslot);
   return 0;
 }

@@ -45,6 +45,7 @@ typedef struct {
   int norm_topk;     /* 1: renormalise the selected weights */
   double rsf;        /* routed_scaling_factor */
   int act_q8_0;      /* 1: Q8_0 int8 activations for every expert matmul */
+  double top_p;      /* 0 < top_p < 1: adaptive expert top-p (lossy, opt-in); else off */
 } orc_config;
 
 /* One expert: int8 containers (code per weight) and fp32 per-row scales. */
@@ -68,12 +69,14 @@ void orc_router_logits(const orc_config *c, const double *x, int T, const float 
 /* Routing of T tokens from their logits.  Writes ids[T][k] (slot order = descending
  * selection score, ties to the lower expert index), w[T][k], and, if margin != NULL,
  * margin[t] = the smallest gap at any decision boundary of token t (see the .c file).
+ * With top_p on, slots past the kept prefix have id -1 and weight 0.
  * bias may be NULL (= zeros).  Returns 0, or -1 on an unsupported config. */
 int orc_route(const orc_config *c, const double *logits, const float *bias, int T,
               int32_t *ids, double *w, double *margin);
 
 /* Canonical permutation: offsets[E+1] (exclusive scan of per-expert counts) and
- * perm[T*k] = slot indices t*k+j ordered by (expert ascending, token ascending). */
+ * perm[T*k] = slot indices t*k+j ordered by (expert ascending, token ascending); slots with
+ * id -1 (dropped by top-p) are left out and the tail of perm is -1. */
 void orc_permutation(int T, int k, int E, const int32_t *ids, int32_t *offsets, int32_t *perm);
 
 /* One SwiGLU expert on n rows of x (fp64 [n][H]) -> y [n][H]. */

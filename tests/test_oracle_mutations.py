@@ -55,6 +55,10 @@ MUTANTS = {
     "quant_truncate": ("const float rr = roundf(ratio);", "const float rr = truncf(ratio);"),
     "rmsnorm_not_rounded": ("xn[(size_t)t * H + h] = round_bf16(rt[h] * inv);",
                             "xn[(size_t)t * H + h] = rt[h] * inv;"),
+    "topp_not_renormalised": ("    for (int j = 0; j < m; j++) wsum += wsrc[sorted[j]];\n",
+                              "    for (int j = 0; j < k; j++) wsum += wsrc[sorted[j]];\n"),
+    "topp_keeps_the_crossing_slot_too": ("      if (before >= c->top_p) break;",
+                                         "      if (before > c->top_p + 0.2) break;"),
 }
 
 

@@ -556,3 +556,88 @@ def test_quantize_properties(bits):
     assert np.all(err <= 0.5 * s[:, None] * (1 + 1e-6))
     q2, s2 = oracle.quantize_rows(w * 2, bits)
     assert np.array_equal(q2, q) and np.array_equal(s2, 2 * s)
+
+
+# ------------------------------------------------------------------ adaptive expert top-p
+# Reading of "Show HN" 实用调节项 (--topp, an explicit lossy override): after the top-k
+# selection, in slot order keep the shortest prefix whose share of the selected weight
+# sources reaches p (at least one expert); dropped slots: id -1, weight 0; kept weights
+# normalised over the kept experts.
+
+def test_topp_off_values_change_nothing():
+    s = _tiny_spec(n_experts=16, top_k=4)
+    lg = np.random.default_rng(21).standard_normal((30, 16)) * 2
+    ref = oracle.route(s, lg)
+    for p in (0.0, 1.0, 1.5):
+        got = oracle.route(s.replace(top_p=p), lg)
+        for a, b in zip(ref, got):
+            assert np.array_equal(a, b)
+
+
+def test_topp_hand_worked_softmax():
+    """p = (0.5, 0.3, 0.15, 0.05), k = 3: shares of the selected mass 0.95 are
+    0.526, 0.316, 0.158; at top_p 0.7 the share before slot 2 is 0.842 >= 0.7, so two
+    experts stay, weighted 0.5 / 0.8 and 0.3 / 0.8."""
+    s = _tiny_spec(n_experts=4, top_k=3, top_p=0.7)
+    lg = np.log(np.array([[0.5, 0.3, 0.15, 0.05]]))
+    ids, w, margin = oracle.route(s, lg)
+    assert list(ids[0]) == [0, 1, -1]
+    assert w[0] == pytest.approx([0.625, 0.375, 0.0], rel=1e-13, abs=0)
+    # the closest decision: the share before the dropped slot (0.8 / 0.95) against 0.7
+    assert margin[0] == pytest.approx(min(0.8 / 0.95 - 0.7, 0.7 - 0.5 / 0.95, 0.15 - 0.05),
+                                      rel=1e-9)
+    ids, w, _ = oracle.route(s.replace(top_p=0.5), lg)  # 0.526 > 0.5 already: one expert
+    assert list(ids[0]) == [0, -1, -1] and w[0] == pytest.approx([1.0, 0.0, 0.0])
+
+
+def test_topp_tiny_p_keeps_one_expert_with_the_whole_weight():
+    s = _tiny_spec(n_experts=16, top_k=4, router="sigmoid_grouped", n_group=4, topk_group=2,
+                   rsf=2.5, top_p=1e-9)
+    lg = np.random.default_rng(22).standard_normal((20, 16))
+    ids0, _, _ = oracle.route(s.replace(top_p=0.0), lg)
+    ids, w, _ = oracle.route(s, lg)
+    assert np.array_equal(ids[:, 0], ids0[:, 0])
+    assert np.all(ids[:, 1:] == -1) and np.all(w[:, 1:] == 0.0)
+    assert np.allclose(w[:, 0], 2.5, rtol=1e-14)
+
+
+@pytest.mark.parametrize("router", ["softmax", "sigmoid_grouped"])
+def test_topp_invariants(router):
+    """Kept prefix: share before its last slot < p <= share of the whole prefix (or all
+    k kept); kept weights sum to rsf; the kept ids are the top-k ids' prefix."""
+    if router == "softmax":
+        s = _tiny_spec(n_experts=16, top_k=6, top_p=0.6)
+    else:
+        s = _tiny_spec(n_experts=32, top_k=6, router="sigmoid_grouped", n_group=4,
+                       topk_group=2, rsf=2.5, top_p=0.6)
+    lg = np.random.default_rng(23).standard_normal((40, s.n_experts)) * 1.5
+    ids0, w0, _ = oracle.route(s.replace(top_p=0.0), lg)
+    ids, w, _ = oracle.route(s, lg)
+    for t in range(40):
+        m = int(np.sum(ids[t] >= 0))
+        assert m >= 1 and np.all(ids[t, m:] == -1) and np.all(w[t, m:] == 0.0)
+        assert np.array_equal(ids[t, :m], ids0[t, :m])
+        share = w0[t] / w0[t].sum()  # w0 is proportional to the weight sources
+        assert share[:m - 1].sum() < 0.6 and (m == s.top_k or share[:m].sum() >= 0.6)
+        assert w[t, :m].sum() == pytest.approx(s.rsf, rel=1e-13)
+        assert np.allclose(w[t, :m] / w[t, :m].sum(), w0[t, :m] / w0[t, :m].sum(), rtol=1e-13)
+
+
+def test_topp_layer_union_equals_per_token_and_drops_experts():
+    s, x, wr, bias, experts, sh = _tiny_layer("sigmoid_grouped", top_p=0.5)
+    i0, w0, o0 = oracle.layer_forward(s, x, wr, bias, experts, sh, mode=0)
+    i1, w1, o1 = oracle.layer_forward(s, x, wr, bias, experts, sh, mode=1)
+    assert np.array_equal(i0, i1) and np.array_equal(w0, w1) and np.array_equal(o0, o1)
+    assert np.any(i1 < 0)
+    off, perm = oracle.permutation(i1, s.n_experts)
+    n = int(np.sum(i1 >= 0))
+    assert off[-1] == n and np.all(perm[n:] == -1)
+    flat = i1.ravel()
+    assert sorted(perm[:n].tolist()) == sorted(np.flatnonzero(flat >= 0).tolist())
+    # the layer equals the plain definition: shared + sum over kept slots of w * expert
+    ref = oracle.expert_forward(s, sh, x)
+    for t in range(x.shape[0]):
+        for j in range(s.top_k):
+            if i1[t, j] >= 0:
+                ref[t] += w1[t, j] * oracle.expert_forward(s, experts[i1[t, j]], x[t:t + 1])[0]
+    assert np.allclose(o1, ref, rtol=1e-12, atol=1e-12)
