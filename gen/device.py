@@ -18,7 +18,7 @@ def config_for(s: G.LayerSpec):
                            n_shared=s.n_shared, inter_shared=s.inter_shared, n_group=s.n_group,
                            topk_group=s.topk_group, norm_topk=s.norm_topk,
                            routed_scaling_factor=s.rsf, weight_bits=s.weight_bits,
-                           act_q8_0=s.act_q8_0)
+                           act_q8_0=s.act_q8_0, expert_top_p=s.top_p)
 
 
 def build_packed_layer(s: G.LayerSpec, seed: int, layer: int = 0, device="cuda", bias=None,

@@ -76,6 +76,12 @@ typedef struct {
   float routed_scaling_factor; /* multiplies the routed weights (1 for softmax layers) */
   int weight_bits;     /* 4, 8 or 2 */
   int act_q8_0;        /* 1 = Q8_0 int8 activations (blocks of 32, fp32 scale) */
+  float expert_top_p;  /* adaptive expert top-p, lossy and opt-in ("Show HN: 如何在我的低配置
+                        * 电脑上运行 GLM-5.2", 实用调节项 --topp): 0 < p < 1 keeps, in slot
+                        * order, the shortest prefix of a token's k selected experts whose
+                        * share of their weight sources reaches p (at least one); dropped
+                        * slots get id -1 and weight 0 and are not computed, and the kept
+                        * weights are normalised over the kept experts.  0 (or >= 1) = off. */
 } moe_layer_config;
 
 /* Source weights for packing: int8 containers (one code per byte, row-major, codes in

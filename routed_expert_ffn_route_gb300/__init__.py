@@ -56,7 +56,7 @@ class moe_layer_config(C.Structure):
                 ("top_k", C.c_int), ("n_shared", C.c_int), ("inter_shared", C.c_int),
                 ("router", C.c_int), ("n_group", C.c_int), ("topk_group", C.c_int),
                 ("norm_topk", C.c_int), ("routed_scaling_factor", C.c_float),
-                ("weight_bits", C.c_int), ("act_q8_0", C.c_int)]
+                ("weight_bits", C.c_int), ("act_q8_0", C.c_int), ("expert_top_p", C.c_float)]
 
 
 class moe_weight_src(C.Structure):
@@ -153,12 +153,12 @@ def _dtype(x) -> int:
 
 def make_config(hidden, inter, n_experts, top_k, router="softmax", n_shared=0, inter_shared=0,
                 n_group=1, topk_group=1, norm_topk=1, routed_scaling_factor=1.0, weight_bits=4,
-                act_q8_0=0) -> moe_layer_config:
+                act_q8_0=0, expert_top_p=0.0) -> moe_layer_config:
     r = {"softmax": MOE_ROUTER_SOFTMAX, "sigmoid_grouped": MOE_ROUTER_SIGMOID_GROUPED}.get(
         router, router)
     return moe_layer_config(hidden, inter, n_experts, top_k, n_shared, inter_shared, int(r),
                             n_group, topk_group, norm_topk, float(routed_scaling_factor),
-                            weight_bits, act_q8_0)
+                            weight_bits, act_q8_0, float(expert_top_p))
 
 
 def moe_version() -> int:

@@ -271,8 +271,10 @@ __global__ void combine_kernel(int T, int H, int k, int n_shared, const float *w
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (n_shared) acc = ((const float4 *)(y + ((long)T * k + t) * H))[c4];
   for (int j = 0; j < k; j++) {
+    const int sp = slot_pos[t * k + j];
+    if (sp < 0) continue;  // dropped by top-p
     float wj = w[t * k + j];
-    float4 v = ((const float4 *)(y + (long)slot_pos[t * k + j] * H))[c4];
+    float4 v = ((const float4 *)(y + (long)sp * H))[c4];
     acc.x = fmaf(wj, v.x, acc.x);
     acc.y = fmaf(wj, v.y, acc.y);
     acc.z = fmaf(wj, v.z, acc.z);

@@ -61,6 +61,7 @@ static int check(const moe_layer_config *c) {
   if (c->weight_bits != 4 && c->weight_bits != 8 && c->weight_bits != 2) return MOE_ERR_UNSUPPORTED;
   if (c->act_q8_0 != 0 && c->act_q8_0 != 1) return MOE_ERR_UNSUPPORTED;
   if (c->act_q8_0 && c->weight_bits != 8) return MOE_ERR_UNSUPPORTED;
+  if (!(c->expert_top_p >= 0.f) || !std::isfinite(c->expert_top_p)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 

@@ -42,7 +42,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
     __syncwarp();
     int t = c * 32 + lane;
     if (t < T)
-      for (int j = 0; j < k; j++) atomicOr(&my[ids[t * k + j]], 1u << lane);
+      for (int j = 0; j < k; j++)
+        if (ids[t * k + j] >= 0) atomicOr(&my[ids[t * k + j]], 1u << lane);
     __syncwarp();
     for (int e = lane; e < E; e += 32) cbase[c * E + e] = (uint16_t)__popc(my[e]);
     __syncwarp();
@@ -98,18 +99,25 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
   const int rbase = n_shared ? T : 0;  // routed rows follow the shared expert's T rows
   if (threadIdx.x == 0) ctrl->n_groups = ns + gstart[E];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets_out[e] = offs[e];
+  // slots dropped by top-p (id -1) are not permuted: the tail of perm is -1
+  for (int i = offs[E] + threadIdx.x; i < T * k; i += blockDim.x) perm[i] = -1;
   // 3. stable scatter
   for (int c = warp; c < n_chunks; c += 32) {
     for (int e = lane; e < E; e += 32) my[e] = 0;
     __syncwarp();
     int t = c * 32 + lane;
     if (t < T)
-      for (int j = 0; j < k; j++) atomicOr(&my[ids[t * k + j]], 1u << lane);
+      for (int j = 0; j < k; j++)
+        if (ids[t * k + j] >= 0) atomicOr(&my[ids[t * k + j]], 1u << lane);
     __syncwarp();
     if (t < T) {
       unsigned below = (1u << lane) - 1u;
       for (int j = 0; j < k; j++) {
         int e = ids[t * k + j];
+        if (e < 0) {  // dropped by top-p
+          slot_pos[t * k + j] = -1;
+          continue;
+        }
         int pos = offs[e] + cbase[c * E + e] + __popc(my[e] & below);
         perm[pos] = t * k + j;
         slot_pos[t * k + j] = pos;

@@ -441,13 +441,30 @@ __device__ __forceinline__ void topk_token(const moe_layer_config &c, const floa
     if (lane == j) { my_id = e_best; my_w = wb; }
   }
   MOE_RT_TRACE(4);
+  // adaptive expert top-p (opt-in): slot j stays while the share of slots 0..j-1 in the
+  // selection's weight sources is below p (slot 0 always); the kept weights are then
+  // normalised over the kept slots
+  bool keep = lane < k;
+  if (c.expert_top_p > 0.f && c.expert_top_p < 1.f) {
+    const float share = lane < k ? my_w / wsum : 0.f;
+    float incl = share;  // inclusive scan of the shares over the slot lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    float before = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) before = 0.f;
+    keep = lane < k && (lane == 0 || before < c.expert_top_p);
+    wsum = warp_sum(keep ? my_w : 0.f);
+  }
   if (lane < k) {
     float v;
     if (c.norm_topk) v = my_w / wsum;
     else v = grouped ? my_w : my_w / sum_all;
-    ids[(long)t * k + lane] = my_id;
-    w[(long)t * k + lane] = v * c.routed_scaling_factor;
-    if (sids) sids[t * k + lane] = my_id;
+    ids[(long)t * k + lane] = keep ? my_id : -1;
+    w[(long)t * k + lane] = keep ? v * c.routed_scaling_factor : 0.f;
+    if (sids) sids[t * k + lane] = keep ? my_id : -1;
   }
   MOE_RT_TRACE(5);
 }
@@ -500,7 +517,7 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
   if (tid < T) sm.tscale[tid] = __ldcg(f.tscale + tid);  // written by the GEMV CTAs
   __syncthreads();
   MOE_FRONT_TRACE(10);
-  if (tid < n) atomicOr(&sm.emask[sm.ids[tid]], 1u << (tid / k));
+  if (tid < n && sm.ids[tid] >= 0) atomicOr(&sm.emask[sm.ids[tid]], 1u << (tid / k));
   __syncthreads();
   // exclusive scans over the experts (thread e): slot offsets and group numbers
   const uint32_t m = tid < E ? sm.emask[tid] : 0u;
@@ -515,13 +532,14 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
   if (lane == 31) sm.wsum[warp] = inc;
   if (lane == 0) sm.wused[warp] = __popc(used);
   __syncthreads();
-  int base = 0, gbase = 0, gtotal = 0;
+  int base = 0, gbase = 0, gtotal = 0, total = 0;
   for (int q = 0; q < kGemvWarps; q++) {
     if (q < warp) {
       base += sm.wsum[q];
       gbase += sm.wused[q];
     }
     gtotal += sm.wused[q];
+    total += sm.wsum[q];
   }
   const int ns = c.n_shared ? (T + GN - 1) / GN : 0;
   const int rbase = c.n_shared ? T : 0;  // routed rows follow the shared expert's T rows
@@ -537,16 +555,18 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
                            0, 0, 0};
   }
   if (tid == 0) {
-    f.offsets[E] = n;
+    f.offsets[E] = total;  // slots kept (all T k unless top-p dropped some)
     ctrl->n_groups = ng;
   }
+  for (int i = total + tid; i < n; i += blockDim.x) f.perm[i] = -1;
   for (int i = tid; i < ns; i += blockDim.x)
     f.groups[i] = Group{E, i * GN, min(GN, T - i * GN), P * i * GN + 7 * i, i * GN + 7 * i,
                         0, 0, 0};
   __syncthreads();
   // stable scatter: slot (t, j) goes after the earlier tokens of its expert; its B rows'
   // 1 / scale go to the rows of its group
-  if (tid < n) {
+  if (tid < n && sm.ids[tid] < 0) f.slot_pos[tid] = -1;  // dropped by top-p
+  if (tid < n && sm.ids[tid] >= 0) {
     const int e = sm.ids[tid], t = tid / k;
     const int r = __popc(sm.emask[e] & ((1u << t) - 1u)), pos = sm.offs[e] + r;
     f.perm[pos] = tid;

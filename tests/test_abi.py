@@ -156,3 +156,11 @@ def test_forward_launch_counts(L):
     q8 = config_for(gen.spec("dsv3_int8"))
     assert moe.moe_forward_launches(q8, 4, bf16) == 7      # Q8_0 encode, no tiles
     assert L.moe_forward_launches(C.byref(dsv3), 7, 1) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_top_p_validation(L):
+    cfg = config_for(gen.spec("dsv3"))
+    for p, ok in ((0.0, True), (0.7, True), (1.0, True), (-0.1, False), (float("nan"), False),
+                  (float("inf"), False)):
+        cfg.expert_top_p = p
+        assert (moe.moe_check_config(cfg) == moe.MOE_OK) == ok, p

@@ -152,6 +152,27 @@ def test_layer_small_grouped_fp32(T):
     check_layer(small("grouped", x_dtype="f32"), T, seed=8)
 
 
+@pytest.mark.parametrize("name,T,p", [("grouped", 7, 0.6), ("grouped", 37, 0.6),
+                                      ("softmax", 9, 0.55), ("grouped_q8", 9, 0.5)])
+def test_layer_small_topp(name, T, p):
+    # adaptive expert top-p: dropped slots (id -1, weight 0) leave the permutation and the
+    # combine; T = 7 runs the fused decode front, T = 37 the separate launches
+    if name == "grouped_q8":
+        s = small("grouped", weight_bits=8, act_q8_0=1, top_p=p)
+    else:
+        s = small(name, top_p=p)
+    _, ids, _, _, _ = check_layer(s, T, seed=10)
+    assert (ids.cpu().numpy() < 0).any()
+
+
+@pytest.mark.parametrize("T,sample", [(1, None), (16, 3), (2048, 2)])
+def test_layer_dsv3_topp(T, sample):
+    out, ids, w, xd, L = check_layer(gen.spec("dsv3").replace(top_p=0.7), T, sample=sample)
+    kept = (ids.cpu().numpy() >= 0).sum(1)
+    print(f"dsv3 top-p 0.7 T={T}: experts kept per token {kept.mean():.2f} of 8")
+    assert kept.min() >= 1
+
+
 def test_layer_decode_rows_without_gemv_router():
     # a hidden size whose router slices do not fit the GEMV at T = 16: the tiled router,
     # selection, permute and token-row launches feed the register-MMA kernels
