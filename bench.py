@@ -418,9 +418,69 @@ def run_ours(a, rank, ws_n, local):
     }
     if not a.no_stack:
         line["stack"] = run_stack(a, rank, ws_n, pk)
+    line["expert_top_p"] = run_topp(s, cfg, packed, seed, rank, pk)
     if rank == 0 and ws_n == 1 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, seed, ntok=4, reps=6)
     return line
+
+
+# ------------------------------------------------------------------ adaptive expert top-p
+
+def run_topp(s, cfg, packed, seed, rank, pk, p=0.7, reps=30):
+    """The same layer and packed weights with adaptive expert top-p (lossy, opt-in) at
+    decode sizes: forward time (CUDA graph replays after an L2 flush, median) and the
+    unique expert bytes actually read, against the lossless forward."""
+    import statistics
+    import numpy as np
+    import torch
+
+    import gen
+    import routed_expert_ffn_route_gb300 as moe
+    from gen.device import hidden_to_device
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    per_expert = expert_bytes(s, s.inter)
+    res = {"p": p, "note": "lossy, opt-in; the headline numbers are the lossless forward"}
+    for T in (1, 16):
+        x, bits = gen.hidden_states(s, seed + 1000 * rank, 50, T)
+        xd = hidden_to_device(s, x, bits)
+        row = {}
+        for name, top_p in (("off", 0.0), ("on", p)):
+            c = type(cfg).from_buffer_copy(cfg)
+            c.expert_top_p = top_p
+            ws = torch.zeros(moe.moe_workspace_bytes(c, T), dtype=torch.uint8, device="cuda")
+            out = torch.empty((T, s.hidden), dtype=torch.float32, device="cuda")
+            ids = torch.empty((T, s.top_k), dtype=torch.int32, device="cuda")
+            w = torch.empty((T, s.top_k), dtype=torch.float32, device="cuda")
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                moe.moe_layer_forward(c, packed, xd, out, ids, w, ws, stream=st)
+                st.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=st):
+                    moe.moe_layer_forward(c, packed, xd, out, ids, w, ws, stream=st)
+                times = []
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                for i in range(reps + 5):
+                    flush.zero_()
+                    e0.record(st)
+                    g.replay()
+                    e1.record(st)
+                    e1.synchronize()
+                    if i >= 5:
+                        times.append(e0.elapsed_time(e1))
+            if moe.moe_read_status(ws) != moe.MOE_OK:
+                raise RuntimeError("device status after the top-p forward")
+            idn = ids.cpu().numpy()
+            uniq = int(np.unique(idn[idn >= 0]).size) + s.n_shared
+            ms = statistics.median(times)
+            row[name] = {"ms": round(ms, 4), "unique_experts": uniq,
+                         "experts_per_token": round(float((idn >= 0).sum(1).mean()), 2),
+                         "expert_bytes": uniq * per_expert,
+                         "hbm_frac_of_measured": round(uniq * per_expert / (ms * 1e-3) / 1e9 /
+                                                       pk["hbm"], 4)}
+        res[f"T{T}"] = row
+    return res
 
 
 # ------------------------------------------------------------------ the stacked layers
