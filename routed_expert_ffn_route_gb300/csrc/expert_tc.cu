@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, 
     const int tok = sh ? g.pos0 + i : perm[g.pos0 + i] / a.k;
     const float sc = tscale[tok];
     if (lane == 0 && part == 0) a.rscale[g.xrow0 + row] = 1.0f / sc;
-#pragma unroll 4
+#pragma unroll 8
     for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr) {
       const size_t col = (size_t)kc * kKChunk + c * 8;
       float f[8];
@@ -663,9 +663,13 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
                                   is_bf16) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
+    // enough CTAs per group to cover the SMs about 8 times over, counted on the groups a
+    // batch usually has (the shared expert's, one per expert in use) rather than the
+    // bound the work list is sized for: most of the grid's rows find no group and exit
     const int rows8_max = round8(a.P * std::min(W.group_n, a.T));
+    const int groups_est = std::min(W.max_groups, a.ns + std::min(a.E, a.T * a.k));
     const int gy = std::max(1, std::min((rows8_max * (a.H / kKChunk / 4) + 63) / 64,
-                                        (8 * d.sms + W.max_groups - 1) / W.max_groups));
+                                        (8 * d.sms + groups_est - 1) / groups_est));
     if (launch_pdl(gather_x_kernel, dim3(W.max_groups, gy), dim3(256), 0, st, a, x, is_bf16,
                    perm, tscale) != cudaSuccess)
       return MOE_ERR_CUDA;

@@ -15,6 +15,8 @@ namespace moe {
 __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(int H, float *r, const float *add,
                                                                const uint16_t *x0, float eps,
                                                                uint16_t *xn) {
+  pdl_wait();  // the layer's combine (its predecessor) has written `add`
+  pdl_trigger();
   const int t = blockIdx.x;
   float *rt = r + (size_t)t * H;
   const float *at = add ? add + (size_t)t * H : nullptr;
@@ -74,7 +76,8 @@ extern "C" int moe_residual_rmsnorm(int T, int H, float *resid, const float *add
   if (!resid || !x_next || ((uintptr_t)resid % 16) || ((uintptr_t)x_next % 16) ||
       (add && ((uintptr_t)add % 16)) || (x0 && ((uintptr_t)x0 % 16)))
     return MOE_ERR_INVALID_ARG;
-  moe::residual_rmsnorm_kernel<<<T, 256, 0, (cudaStream_t)stream>>>(H, resid, add, x0, eps,
-                                                                     x_next);
+  if (moe::launch_pdl(moe::residual_rmsnorm_kernel, dim3(T), dim3(256), 0, (cudaStream_t)stream,
+                      H, resid, add, x0, eps, x_next) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
