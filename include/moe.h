@@ -142,7 +142,9 @@ int moe_unpack_weights(const moe_layer_config *cfg, const void *packed, int expe
  * x [T][H] (fp32 or bf16, per `dtype`) -> ids [T][k] int32 in slot order (descending
  * selection score, ties to the lower expert index) and w [T][k] fp32 routed weights
  * (softmax: p / sum of selected p; grouped: sigmoid / sum of selected sigmoids, times
- * routed_scaling_factor).  T == 0 is a no-op.  T <= the workspace's max_tokens. */
+ * routed_scaling_factor).  With expert_top_p on, the slots it drops have id -1 and
+ * weight 0 and the sums run over the kept slots.  T == 0 is a no-op.  T <= the
+ * workspace's max_tokens. */
 int moe_route_topk(const moe_layer_config *cfg, const void *packed, const void *x,
                    moe_dtype dtype, int T, int32_t *ids, float *w, void *ws, size_t ws_bytes,
                    void *stream);
@@ -159,8 +161,10 @@ int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const voi
  * passed as void*) on `stream` around the stages, events[0] before the first kernel and
  * events[i+1] after stage i, for the stages 0 router (logits + top-k), 1 permutation,
  * 2 activation encoding (Q8_0 codes with act_q8_0, else the fp16 tensor-core tiles),
- * 3 gate/up + SwiGLU, 4 down projection, 5 combine.  n_events must be >= 7.  Same results
- * as moe_layer_forward.  The call may be captured into a CUDA graph: while the stream is
+ * 3 gate/up + SwiGLU, 4 down projection, 5 combine.  Decode-sized batches (every gate/up
+ * group at most 16 activation rows, router on the GEMV) run selection, permutation and
+ * the fp16 token rows inside the router's launch, so stage 0 covers them and stages 1-2
+ * are empty.  n_events must be >= 7.  Same results as moe_layer_forward.  The call may be captured into a CUDA graph: while the stream is
  * capturing, the events are recorded as graph nodes (cudaEventRecordExternal), so each
  * replay records them. */
 int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, const void *x,
@@ -199,7 +203,8 @@ int moe_read_status(void *ws, void *stream);
 
 /* Debug: copy the permutation of the last call that used `ws` (T tokens):
  * offsets [E+1] (exclusive scan of per-expert token counts) and perm [T*k] (slot
- * indices t*k+j ordered by expert, then token).  Device pointers; stream-ordered. */
+ * indices t*k+j ordered by expert, then token; with expert_top_p the slots it dropped are
+ * left out and the tail of perm is -1).  Device pointers; stream-ordered. */
 int moe_debug_permutation(const moe_layer_config *cfg, const void *ws, int T, int32_t *offsets,
                           int32_t *perm, void *stream);
 

@@ -6,12 +6,16 @@
 // used by a few tokens only, the layer is bound by streaming the codes from HBM, and the
 // work per byte is small: the kernel keeps HBM busy with the fewest hand-offs.
 //
-//  - One producer thread per CTA streams runs of up to 4 code chunks (16 KB at int4) and
-//    the matching activation-tile chunks, one bulk copy each, into a ring of stages.
+//  - One producer warp per CTA streams runs of up to 4 code chunks (16 KB at int4, one
+//    bulk copy) into a ring of stages, with the run's activations: for gate/up one bulk
+//    copy per group row from the per-token fp16 rows written in front of the launch (rows
+//    padded by 16 bytes in the stage against bank conflicts), for down the run's chunks
+//    of the group's h tile.  Launched as a programmatic dependent, the down kernel issues
+//    its first code copies before the gate/up grid has finished.
 //  - Eight compute warps each own 16 of the item's 128 weight rows for the whole K loop:
 //    codes go from shared memory to registers, are dequantised (exact small integers in
-//    fp16) straight into the A fragments of mma.sync m16n8k16, the fp16 activation tile
-//    gives the B fragments, and the fp32 accumulators stay in registers (two chains per
+//    fp16) straight into the A fragments of mma.sync m16n8k16, the fp16 activations give
+//    the B fragments, and the fp32 accumulators stay in registers (two chains per
 //    8-token tile, even and odd k-steps, to halve the MMA dependency chain).
 //  - A run's chunk count is a template constant, so the chunk loop unrolls and the
 //    compiler overlaps one chunk's loads and dequantisation with the previous MMAs.
