@@ -340,7 +340,7 @@ template <int BITS, bool DOWN, int NT, int RA>
 static int launch_mma(const TcArgs &a, int bound, int sms, cudaStream_t st) {
   auto k = mma_expert_kernel<BITS, DOWN, NT, RA>;
   constexpr size_t smem = MmaPlan<BITS>::smem;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  set_dyn_smem((const void *)k, (int)smem);
   const int grid = 2 * sms < bound ? 2 * sms : bound;  // two CTAs per SM
   if (launch_pdl(k, dim3(grid), dim3(kMmaThreads), smem, st, a, bound) != cudaSuccess)
     return MOE_ERR_CUDA;

@@ -318,9 +318,8 @@ static int launch_persistent(K kern, size_t smem, int item_bound, const ExpertAr
   if (item_bound <= 0) return MOE_OK;
   DevInfo d = dev_info();
   if ((long)smem > d.smem_optin) return MOE_ERR_UNSUPPORTED;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  int per_sm = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+  set_dyn_smem((const void *)kern, (int)smem);
+  int per_sm = cached_blocks_per_sm((const void *)kern, 256, smem);
   if (per_sm < 1) per_sm = 1;
   int grid = d.sms * per_sm;
   if (grid > item_bound) grid = item_bound;

@@ -591,14 +591,14 @@ static int launch_tc(const TcArgs &a, int bound, int sms, bool pairs, cudaStream
   constexpr size_t smem = tc_smem<NMAX, BITS>();
   if (!pairs) {
     auto k = tc_expert_kernel<BITS, DOWN, NMAX, 1>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_dyn_smem((const void *)k, (int)smem);
     if (launch_pdl(k, dim3(bound < sms ? bound : sms), dim3(kThreads), smem, st, a, bound) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
   auto k = tc_expert_kernel<BITS, DOWN, NMAX, 2>;
-  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  set_dyn_smem((const void *)k, (int)smem);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -613,10 +613,9 @@ static int launch_tc(const TcArgs &a, int bound, int sms, bool pairs, cudaStream
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
   // as many clusters as can be resident at once (both CTAs of a cluster share a GPC)
-  int clusters = 0;
   cfg.gridDim = dim3(2 * (sms / 2));
-  if (cudaOccupancyMaxActiveClusters(&clusters, k, &cfg) != cudaSuccess || clusters < 1)
-    clusters = sms / 2;
+  int clusters = cached_active_clusters((const void *)k, cfg);
+  if (clusters < 1) clusters = sms / 2;
   const int pairs_total = bound / 2;  // bound is even: every group has an even m-tile count
   cfg.gridDim = dim3(2 * std::min(clusters, pairs_total));
   cfg.numAttrs = 2;

@@ -3,10 +3,64 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "moe_internal.cuh"
 
 namespace moe {
+
+// Host-side per-launch work cached per (kernel, device): the dynamic shared-memory limit
+// (the attribute persists once set) and occupancy queries (fixed for a kernel and launch
+// shape), so an eager forward costs little more host time than its launches.
+static uint64_t func_key(const void *func, int extra) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return ((uint64_t)(uintptr_t)func * 1000003ull) ^ ((uint64_t)dev << 56) ^ (uint64_t)extra;
+}
+
+void set_dyn_smem(const void *func, int bytes) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> done;
+  const uint64_t key = func_key(func, 0);
+  std::lock_guard<std::mutex> g(mu);
+  auto it = done.find(key);
+  if (it != done.end() && it->second >= bytes) return;
+  cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  done[key] = bytes;
+}
+
+template <typename Q>
+static int cached(const void *func, int shape, Q query) {
+  static std::mutex mu;
+  static std::unordered_map<uint64_t, int> memo;
+  const uint64_t key = func_key(func, shape);
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+  }
+  const int v = query();
+  std::lock_guard<std::mutex> g(mu);
+  memo[key] = v;
+  return v;
+}
+
+int cached_blocks_per_sm(const void *func, int threads, size_t smem) {
+  return cached(func, (int)smem ^ (threads << 20), [&]() {
+    int v = 0;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, func, threads, smem) == cudaSuccess
+               ? v
+               : 0;
+  });
+}
+
+int cached_active_clusters(const void *func, const cudaLaunchConfig_t &cfg) {
+  // distinct from the blocks-per-SM entries of the same kernel (bit 30)
+  return cached(func, (int)cfg.dynamicSmemBytes ^ (1 << 30), [&]() {
+    int v = 0;
+    return cudaOccupancyMaxActiveClusters(&v, func, &cfg) == cudaSuccess ? v : 0;
+  });
+}
 
 DevInfo dev_info() {
   static std::mutex mu;

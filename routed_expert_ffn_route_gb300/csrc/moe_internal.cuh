@@ -244,6 +244,11 @@ struct DevInfo {
   int smem_optin;
 };
 DevInfo dev_info();
+// Per (kernel, device) host-side caches: the dynamic shared-memory limit is raised once;
+// occupancy answers are computed once per launch shape.
+void set_dyn_smem(const void *func, int bytes);
+int cached_blocks_per_sm(const void *func, int threads, size_t smem);
+int cached_active_clusters(const void *func, const cudaLaunchConfig_t &cfg);
 
 // kernels (one translation unit each)
 // fused: the decode front (selection, permutation and activation rows in the GEMV launch)

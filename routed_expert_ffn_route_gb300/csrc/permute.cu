@@ -149,7 +149,7 @@ int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t
   DevInfo d = dev_info();
   if ((long)smem > d.smem_optin) return MOE_ERR_UNSUPPORTED;
   if (smem > 48 * 1024)
-    cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set_dyn_smem((const void *)permute_kernel, (int)smem);
   if (launch_pdl(permute_kernel, dim3(1), dim3(1024), smem, st, T, c.top_k, c.n_experts,
                  c.n_shared, W.group_n, W.pieces, ids, (int32_t *)(ws + W.offsets),
                  (int32_t *)(ws + W.perm), (int32_t *)(ws + W.slot_pos), (Group *)(ws + W.groups),

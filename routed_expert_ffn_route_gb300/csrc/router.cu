@@ -784,7 +784,7 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
     }
     // the dynamic x slice plus the block's static arrays may pass the 48 KB default
     auto launch = [&](auto k) {
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      set_dyn_smem((const void *)k, (int)smem);
       k<<<grid, kGemvThreads, smem, st>>>(c, packed, wr, x, is_bf16, T, partials, ctrl, xmax,
                                           fused ? 1 : 0, f);
     };

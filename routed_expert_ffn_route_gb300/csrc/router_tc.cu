@@ -195,8 +195,7 @@ int launch_router_tc(const moe_layer_config &c, const uint8_t *packed, const voi
           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return MOE_ERR_CUDA;
-  cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)kRtSmem);
+  set_dyn_smem((const void *)router_tc_kernel, (int)kRtSmem);
   router_tc_kernel<<<dim3(MT, NT, hsplits), 128, kRtSmem, st>>>(
       xmap, c, packed, packed + P.router_t_off, T, KC, KC / hsplits, partials, ctrl,
       2000000000L);
