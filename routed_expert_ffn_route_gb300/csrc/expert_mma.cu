@@ -10,8 +10,9 @@
 //    bulk copy) into a ring of stages, with the run's activations: for gate/up one bulk
 //    copy per group row from the per-token fp16 rows written in front of the launch (rows
 //    padded by 16 bytes in the stage against bank conflicts), for down the run's chunks
-//    of the group's h tile.  Launched as a programmatic dependent, the down kernel issues
-//    its first code copies before the gate/up grid has finished.
+//    of the group's h tile.  Launched as programmatic dependents, the gate/up kernel
+//    prefetches the shared expert's codes into L2 while the router still selects, and the
+//    down kernel issues its first code copies before the gate/up grid has finished.
 //  - Eight compute warps each own 16 of the item's 128 weight rows for the whole K loop:
 //    codes go from shared memory to registers, are dequantised (exact small integers in
 //    fp16) straight into the A fragments of mma.sync m16n8k16, the fp16 activations give
@@ -169,7 +170,16 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
       if (!waited) release(run < S ? run : S);
     } else {
       // Gate/up: lane 0 copies each run of codes, lane r the run's slice of group row r
-      // (its token's fp16 row, or row piece, written in front of this launch).
+      // (its token's fp16 row, or row piece, written in front of this launch).  The shared
+      // expert's items do not depend on the routing, so before waiting for the router, lane
+      // 0 of a CTA that will take one warms L2 with the item's codes: the router's selection
+      // runs in a single CTA and leaves HBM idle meanwhile.
+      if (lane == 0 && a.ns) {
+        const int mt_s = a.LS.inter / 64, kc = a.H / kKChunk;
+        for (int item = blockIdx.x; item < a.ns * mt_s && item < item_bound; item += gridDim.x)
+          tc::bulk_prefetch_l2(a.shared + a.LS.gu_off + (size_t)(item % mt_s) * kc * AB,
+                               (uint32_t)kc * AB);
+      }
       pdl_wait();
       pdl_trigger();
       Item it;
