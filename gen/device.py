@@ -22,10 +22,13 @@ def config_for(s: G.LayerSpec):
 
 
 def build_packed_layer(s: G.LayerSpec, seed: int, layer: int = 0, device="cuda", bias=None,
-                       packed=None):
+                       packed=None, host_codes=False):
     """Pack the seeded layer (router + all experts + shared) into a device buffer.
 
     bias: optional host fp32 [E] overriding the spec's N(0, bias_std) bias.
+    host_codes: draw the weight codes on the host (numpy) and upload them, instead of
+    drawing them on the device (same values; a few copies instead of many small device
+    kernels, for small layers).
     Returns (cfg, packed uint8 tensor)."""
     import torch
     import routed_expert_ffn_route_gb300 as moe
@@ -45,6 +48,10 @@ def build_packed_layer(s: G.LayerSpec, seed: int, layer: int = 0, device="cuda",
         for which in ("gate", "up", "down"):
             rows, cols = G.expert_rows_cols(s, which, shared=(e >= s.n_experts))
             key = (which, rows, cols)
+            if host_codes:
+                mats[which] = torch.from_numpy(
+                    np.ascontiguousarray(G.expert_codes(s, seed, layer, e, which))).to(device)
+                continue
             if key not in bufs:
                 bufs[key] = torch.empty((rows, cols), dtype=torch.int8, device=device)
             mats[which] = G.expert_codes_torch(s, seed, layer, e, which, device, out=bufs[key])

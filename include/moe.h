@@ -157,6 +157,25 @@ int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const voi
                       moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
                       size_t ws_bytes, void *stream);
 
+/* Expert-parallel share of the layer ("Show HN: 如何在我的低配置电脑上运行 GLM-5.2",
+ * 实验性常驻 CUDA 后端: whole experts are placed on devices, an expert is never split; the
+ * per-device partial results are added): the router and the permutation run over every
+ * expert as in moe_layer_forward, and ids / w receive the full routing, but only routed
+ * experts e with expert_begin <= e < expert_end (and the shared expert when with_shared is
+ * 1) are computed:
+ *   out[t] = [with_shared] shared(x_t) + sum over j with ids[t][j] in [begin, end) of
+ *            w[t][j] * expert_{ids[t][j]}(x_t),   fp32 [T][H].
+ * Devices that own disjoint expert ranges covering [0, E), exactly one of them with the
+ * shared expert, produce partial outputs whose sum is moe_layer_forward's output (up to
+ * the order of the fp32 additions).  Only the owned experts' regions of `packed` are read
+ * (the router weights and the header always are), so a device may pack just its own
+ * experts.  0 <= expert_begin <= expert_end <= n_experts and with_shared in {0, 1}, else
+ * MOE_ERR_INVALID_ARG; everything else as moe_layer_forward (same workspace size). */
+int moe_layer_forward_experts(const moe_layer_config *cfg, const void *packed, const void *x,
+                              moe_dtype dtype, int T, int expert_begin, int expert_end,
+                              int with_shared, float *out, int32_t *ids, float *w, void *ws,
+                              size_t ws_bytes, void *stream);
+
 /* moe_layer_forward with stage timing: records the caller's CUDA events (cudaEvent_t
  * passed as void*) on `stream` around the stages, events[0] before the first kernel and
  * events[i+1] after stage i, for the stages 0 router (logits + top-k), 1 permutation,
@@ -178,16 +197,21 @@ int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, con
  * library's interface, not of the method.
  * Same kernels and results as moe_layer_forward; the scratch is a file-scope device array
  * of 32 MiB inside the library, held by every GPU that loads the library until the
- * process exits.  Calls whose workspace (moe_workspace_bytes(cfg, T)) exceeds 32 MiB are
- * rejected with MOE_ERR_WORKSPACE (for the DeepSeek-V3-style layer: T <= 16).  The first
+ * process exits.  Calls are accepted while their workspace (moe_workspace_bytes(cfg, T)) fits
+ * in 32 MiB, larger ones are rejected with MOE_ERR_WORKSPACE before any launch (for the
+ * DeepSeek-V3-style layer, H = 6144, I = 2048, 256 experts, top-8: T <= 23).  The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  No cudaMalloc,
+ * device current and keeps it for later calls on that device; make that first call before
+ * any stream capture.  The kept address does not survive cudaDeviceReset (the library's
+ * module may load at another address in the new context): do not call this entry point
+ * after resetting a device it was used on.  No cudaMalloc,
  * cudaFree or allocating routine is called.  All calls on a device share the one array,
  * which keeps the last call's contents (each call clears the status word it uses first):
  * calls that overlap on the GPU (issued on different streams, or from several host
  * threads without ordering) race on it, so serialise them.  status: optional device int32 that receives the
  * device status word (MOE_OK, MOE_ERR_NUMERIC, MOE_ERR_PACKED ...) at the end of the call,
- * stream-ordered; may be NULL. */
+ * stream-ordered; may be NULL.  It is written only when the call returns MOE_OK: after an
+ * error return it keeps whatever it held. */
 int moe_layer_forward_static(const moe_layer_config *cfg, const void *packed, const void *x,
                              moe_dtype dtype, int T, float *out, int32_t *ids, float *w,
                              int32_t *status, void *stream);

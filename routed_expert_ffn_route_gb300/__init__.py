@@ -18,7 +18,7 @@ __all__ = [
     "moe_workspace_bytes", "moe_pack_weights", "moe_pack_router", "moe_pack_expert",
     "moe_unpack_weights", "moe_route_topk", "moe_layer_forward", "moe_read_status",
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
-    "moe_debug_wait_timeout", "EXPORTED",
+    "moe_debug_wait_timeout", "moe_layer_forward_experts", "EXPORTED",
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE",
     "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT", "MOE_ERR_NUMERIC", "MOE_ERR_PACKED",
 ]
@@ -39,6 +39,7 @@ EXPORTED = [
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
     "moe_debug_wait_timeout", "moe_layer_forward_timed", "moe_forward_launches",
     "moe_layer_forward_static", "moe_residual_rmsnorm", "moe_quantize_rows",
+    "moe_layer_forward_experts",
 ]
 
 # stages bracketed by the events of moe_layer_forward_timed
@@ -112,6 +113,7 @@ def _bind(L):
         "moe_layer_forward_static": (I, [P, P, P, I, I, P, P, P, P, P]),
         "moe_residual_rmsnorm": (I, [I, I, P, P, P, C.c_float, P, P]),
         "moe_quantize_rows": (I, [P, I, I, I, I, P, P, P]),
+        "moe_layer_forward_experts": (I, [P, P, P, I, I, I, I, I, P, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -216,6 +218,16 @@ def moe_layer_forward(cfg, packed, x, out, ids, w, ws, stream=None):
     T = x.shape[0]
     _ck(lib().moe_layer_forward(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out), _p(ids),
                                 _p(w), _p(ws), ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_experts(cfg, packed, x, expert_begin, expert_end, with_shared, out, ids,
+                              w, ws, stream=None):
+    """Expert-parallel share: out = [shared] + the routed experts in [begin, end) only."""
+    T = x.shape[0]
+    _ck(lib().moe_layer_forward_experts(C.byref(cfg), _p(packed), _p(x), _dtype(x), T,
+                                        int(expert_begin), int(expert_end), int(with_shared),
+                                        _p(out), _p(ids), _p(w), _p(ws), ws.numel(),
+                                        _stream(stream)), "moe_layer_forward_experts")
 
 
 def moe_layer_forward_timed(cfg, packed, x, out, ids, w, ws, events, stream=None):

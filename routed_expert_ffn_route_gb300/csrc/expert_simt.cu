@@ -16,7 +16,8 @@
 // contiguous bytes (int4) per chunk.
 //
 // Combine ("colibrì 深度拆解", §4.3): out[t] = shared(x_t) + sum_j w[t][j] * y(t, j), summed in
-// slot order; one thread per 4 outputs, no atomics, so results are bit-reproducible.
+// slot order; one thread per 4 outputs, no atomics, so results are bit-reproducible.  Slots
+// without an output row (dropped by top-p, or outside an expert-parallel share) are skipped.
 #include "dev.cuh"
 #include "moe_internal.cuh"
 
@@ -272,7 +273,7 @@ __global__ void combine_kernel(int T, int H, int k, int n_shared, const float *w
   if (n_shared) acc = ((const float4 *)(y + ((long)T * k + t) * H))[c4];
   for (int j = 0; j < k; j++) {
     const int sp = slot_pos[t * k + j];
-    if (sp < 0) continue;  // dropped by top-p
+    if (sp < 0) continue;  // dropped by top-p, or an expert outside the call's share
     float wj = w[t * k + j];
     float4 v = ((const float4 *)(y + (long)sp * H))[c4];
     acc.x = fmaf(wj, v.x, acc.x);
@@ -290,7 +291,7 @@ static ExpertArgs make_args(const moe_layer_config &c, const uint8_t *packed, co
   ExpertArgs a{};
   a.routed = packed + P.experts_off;
   a.routed_stride = P.routed.bytes;
-  a.shared = c.n_shared ? packed + P.shared_off : nullptr;
+  a.shared = c.n_shared && W.shared ? packed + P.shared_off : nullptr;
   a.LR = P.routed;
   a.LS = P.shared;
   a.H = c.hidden;
@@ -304,7 +305,7 @@ static ExpertArgs make_args(const moe_layer_config &c, const uint8_t *packed, co
   a.perm = (const int32_t *)(ws + W.perm);
   a.groups = (const Group *)(ws + W.groups);
   a.ctrl = (const Ctrl *)(ws + W.ctrl);
-  a.ns = c.n_shared ? (T + W.group_n - 1) / W.group_n : 0;
+  a.ns = c.n_shared && W.shared ? (T + W.group_n - 1) / W.group_n : 0;
   a.h = (float *)(ws + W.h);
   a.y = (float *)(ws + W.y);
   a.xq = (const int8_t *)(ws + W.xq);
@@ -377,7 +378,7 @@ int launch_combine(const moe_layer_config &c, int T, const float *w, float *out,
                    const WsLayout &W, cudaStream_t st) {
   long n = (long)T * (c.hidden / 4);
   if (launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, T, c.hidden,
-                 c.top_k, c.n_shared, w, (const int32_t *)(ws + W.slot_pos),
+                 c.top_k, c.n_shared && W.shared ? 1 : 0, w, (const int32_t *)(ws + W.slot_pos),
                  (const float *)(ws + W.y), out) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

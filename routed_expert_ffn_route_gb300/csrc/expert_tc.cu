@@ -173,11 +173,9 @@ struct RunPos {
   }
 };
 
-// CL = 2: CTAs run in clusters of two that take adjacent m-tiles of the same group (items
-// 2p and 2p + 1), so that they read the same activation tiles: each run of tiles is loaded
-// once, by the two CTAs in turn, and multicast into both; a ring stage is refilled once
-// both CTAs' MMAs have released it.
-template <int BITS, bool DOWN, int NMAX, int CL>
+// Consecutive CTAs take adjacent m-tiles of a group, which read the same activation tiles:
+// each CTA loads its own copy of them (the group's first reader brings them into L2).
+template <int BITS, bool DOWN, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int item_bound) {
   using PL = Plan<NMAX>;
   using RG = Rings<NMAX, BITS>;
@@ -203,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     }
     for (int s = 0; s < SB; s++) {
       tc::mbar_init(&bars->b_full[s], 1);
-      tc::mbar_init(&bars->b_empty[s], CL * (rb < NI ? rb : NI));  // each CTA's issuers
+      tc::mbar_init(&bars->b_empty[s], rb < NI ? rb : NI);  // the issuers
     }
     for (int s = 0; s < ST; s++) {
       tc::mbar_init(&bars->t_full[s], 4);  // the set's 4 warps
@@ -220,11 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   if (warp == 0) tc::tmem_alloc<512>(&bars->tmem_base);
   tc::fence_before_sync();
   __syncthreads();
-  if (CL == 2) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::fence_after_sync();
   pdl_wait();  // the set-up above overlaps the previous launch; the work list is its output
   pdl_trigger();
-  const uint32_t crank = CL == 2 ? tc::cluster_rank() : 0;
   const uint32_t tbase = bars->tmem_base;
   volatile int *abort = &bars->abort_flag;
   const long lim = a.wait_limit;
@@ -248,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         if (!tc_item<DOWN>(a, item, it)) break;
         // the item's activation tiles are one contiguous range, read again by the group's
         // other m-tiles: start it towards L2 now, so that the ring's copies hit L2
-        if (!isA && CL == 1)
+        if (!isA)
           tc::bulk_prefetch_l2(b_src<DOWN>(a, it, 0), (uint32_t)it.KC * it.rows8 * 128);
         for (int kc = 0; kc < it.KC; kc += R, run++, pos.next(S)) {
           const int s = pos.s;
@@ -261,11 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
           } else {
             const uint32_t bytes = (uint32_t)R * it.rows8 * 128;
             tc::mbar_arrive_expect_tx(&full[s], bytes);  // every run lands here
-            if (CL == 1)
-              tc::bulk_g2s(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes, &full[s]);
-            else if ((uint32_t)(run & 1) == crank)  // runs alternate between the two CTAs
-              tc::bulk_g2s_multicast(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes,
-                                     &full[s], 0x3);
+            tc::bulk_g2s(bring + s * b_stride, b_src<DOWN>(a, it, kc), bytes, &full[s]);
             MOE_TC_TRACE(1, run * R);
           }
           armed |= 1u << s;
@@ -322,10 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
               for (int kk = 0; kk < 4; kk++)
                 tc::mma_ts(dcol, acol + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
                            ku + j + kk > 0);
-              if (last_of_run) {  // the run's last chunk: release the stage (in both CTAs)
-                if (CL == 1) tc::mma_commit(&bars->b_empty[bpos.r.s]);
-                else tc::mma_commit_multicast(&bars->b_empty[bpos.r.s], 0x3);
-              }
+              if (last_of_run) tc::mma_commit(&bars->b_empty[bpos.r.s]);  // release the stage
             }
           }
           if (leader) {
@@ -499,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc<512>(tbase);
-  if (CL == 2) tc::cluster_sync();  // no copy or arrival from the peer is still due here
 }
 
 // x -> the gate/up B tiles: per group, [k-chunk][rows rounded up to 8][128-byte swizzled
@@ -587,55 +575,26 @@ __global__ void __launch_bounds__(256) token_rows_kernel(TcArgs a, const void *x
 }
 
 template <int BITS, bool DOWN, int NMAX>
-static int launch_tc(const TcArgs &a, int bound, int sms, bool pairs, cudaStream_t st) {
+static int launch_tc(const TcArgs &a, int bound, int sms, cudaStream_t st) {
   constexpr size_t smem = tc_smem<NMAX, BITS>();
-  if (!pairs) {
-    auto k = tc_expert_kernel<BITS, DOWN, NMAX, 1>;
-    set_dyn_smem((const void *)k, (int)smem);
-    if (launch_pdl(k, dim3(bound < sms ? bound : sms), dim3(kThreads), smem, st, a, bound) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-  }
-  auto k = tc_expert_kernel<BITS, DOWN, NMAX, 2>;
+  auto k = tc_expert_kernel<BITS, DOWN, NMAX>;
   set_dyn_smem((const void *)k, (int)smem);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
-  // as many clusters as can be resident at once (both CTAs of a cluster share a GPC)
-  cfg.gridDim = dim3(2 * (sms / 2));
-  int clusters = cached_active_clusters((const void *)k, cfg);
-  if (clusters < 1) clusters = sms / 2;
-  const int pairs_total = bound / 2;  // bound is even: every group has an even m-tile count
-  cfg.gridDim = dim3(2 * std::min(clusters, pairs_total));
-  cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, k, a, bound) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_pdl(k, dim3(bound < sms ? bound : sms), dim3(kThreads), smem, st, a, bound) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 // NMAX: the smallest supported width >= the largest B row count of any group in the launch
 template <int BITS, bool DOWN>
 static int launch_tc_n(TcArgs a, int rows_max, int kc_gcd, int bound, int sms, cudaStream_t st) {
-  // CTA pairs share activation tiles when every group has an even number of m-tiles
-  const bool pairs = DOWN ? (a.H / 128) % 2 == 0
-                          : (a.LR.inter / 64) % 2 == 0 && (a.LS.inter / 64) % 2 == 0;
   // chunks per copy: code runs of 4 chunks (16 KB at int4) where every K allows it;
   // activation tiles in runs too when they are small (decode), else one chunk per copy
   a.ra = kc_gcd % 4 == 0 ? 4 : (kc_gcd % 2 == 0 ? 2 : 1);
   a.rb = rows_max <= 32 ? a.ra : 1;
-  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32>(a, bound, sms, pairs, st);
-  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64>(a, bound, sms, pairs, st);
-  return launch_tc<BITS, DOWN, 128>(a, bound, sms, pairs, st);
+  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32>(a, bound, sms, st);
+  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64>(a, bound, sms, st);
+  return launch_tc<BITS, DOWN, 128>(a, bound, sms, st);
 }
 
 static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
@@ -697,7 +656,7 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   TcArgs a{};
   a.routed = packed + P.experts_off;
   a.routed_stride = P.routed.bytes;
-  a.shared = c.n_shared ? packed + P.shared_off : nullptr;
+  a.shared = c.n_shared && W.shared ? packed + P.shared_off : nullptr;
   a.LR = P.routed;
   a.LS = P.shared;
   a.H = c.hidden;
@@ -709,7 +668,7 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   a.P = W.pieces;
   a.groups = (const Group *)(ws + W.groups);
   a.ctrl = (Ctrl *)(ws + W.ctrl);
-  a.ns = c.n_shared ? (T + W.group_n - 1) / W.group_n : 0;
+  a.ns = c.n_shared && W.shared ? (T + W.group_n - 1) / W.group_n : 0;
   a.xg = ws + W.xg;
   a.xt = ws + W.xg;  // decode-sized forwards use the region for token rows instead
   a.tscale = (const float *)(ws + W.tscale);

@@ -54,14 +54,6 @@ int cached_blocks_per_sm(const void *func, int threads, size_t smem) {
   });
 }
 
-int cached_active_clusters(const void *func, const cudaLaunchConfig_t &cfg) {
-  // distinct from the blocks-per-SM entries of the same kernel (bit 30)
-  return cached(func, (int)cfg.dynamicSmemBytes ^ (1 << 30), [&]() {
-    int v = 0;
-    return cudaOccupancyMaxActiveClusters(&v, func, &cfg) == cudaSuccess ? v : 0;
-  });
-}
-
 DevInfo dev_info() {
   static std::mutex mu;
   static DevInfo cache[64];
@@ -267,12 +259,20 @@ int moe_route_topk(const moe_layer_config *cfg, const void *packed, const void *
   return launch_router(*cfg, (const uint8_t *)packed, x, dtype, T, ids, w, (uint8_t *)ws, W, st);
 }
 
+// One forward; share (optional): {e0, e1, shared} restricts the computed experts to an
+// expert-parallel share of the layer.
 static int forward_impl(const moe_layer_config *cfg, const void *packed, const void *x,
                         moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
-                        size_t ws_bytes, void *const *ev, void *stream) {
+                        size_t ws_bytes, void *const *ev, void *stream,
+                        const int *share = nullptr) {
   WsLayout W;
   int r = common_args(cfg, packed, x, dtype, T, ids, w, ws, ws_bytes, &W);
   if (r || T == 0) return r;
+  if (share) {
+    W.e0 = share[0];
+    W.e1 = share[1];
+    W.shared = share[2] != 0 && cfg->n_shared != 0;
+  }
   if (!out || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t *wsb = (uint8_t *)ws;
@@ -302,6 +302,20 @@ int moe_layer_forward(const moe_layer_config *cfg, const void *packed, const voi
                       moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
                       size_t ws_bytes, void *stream) {
   return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_layer_forward_experts(const moe_layer_config *cfg, const void *packed, const void *x,
+                              moe_dtype dtype, int T, int expert_begin, int expert_end,
+                              int with_shared, float *out, int32_t *ids, float *w, void *ws,
+                              size_t ws_bytes, void *stream) {
+  int r = check(cfg);
+  if (r) return r;
+  if (expert_begin < 0 || expert_end < expert_begin || expert_end > cfg->n_experts ||
+      (with_shared != 0 && with_shared != 1))
+    return MOE_ERR_INVALID_ARG;
+  const int share[3] = {expert_begin, expert_end, with_shared};
+  return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, nullptr, stream,
+                      share);
 }
 
 int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, const void *x,

@@ -121,6 +121,11 @@ struct WsLayout {
       y, total;
   int max_groups, group_n, rows, pieces;
   bool tc;
+  // The experts this call computes: routed experts [e0, e1) and, when `shared` is set, the
+  // shared expert (an expert-parallel share of the layer; the whole layer by default).
+  // The routing and the permutation always cover every expert.
+  int e0, e1;
+  bool shared;
 };
 
 int choose_group_n(const moe_layer_config &c, int T);
@@ -138,6 +143,9 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   int gn_min = W.tc ? kTcMaxRows / 2 : choose_group_n(c, T);
   W.group_n = W.tc ? kTcMaxRows / pieces : gn_min;
   W.rows = T * k + (c.n_shared ? T : 0);
+  W.e0 = 0;
+  W.e1 = c.n_experts;
+  W.shared = c.n_shared != 0;
   int tk = T * k;
   W.max_groups = (tk + gn_min - 1) / gn_min + (c.n_experts < tk ? c.n_experts : tk) +
                  (c.n_shared ? (T + gn_min - 1) / gn_min : 0) + 1;
@@ -248,7 +256,6 @@ DevInfo dev_info();
 // occupancy answers are computed once per launch shape.
 void set_dyn_smem(const void *func, int bytes);
 int cached_blocks_per_sm(const void *func, int threads, size_t smem);
-int cached_active_clusters(const void *func, const cudaLaunchConfig_t &cfg);
 
 // kernels (one translation unit each)
 // fused: the decode front (selection, permutation and activation rows in the GEMV launch)

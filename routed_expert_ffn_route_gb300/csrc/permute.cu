@@ -11,7 +11,8 @@
 //     popc(mask & lanes-below), so perm lists t*k+j ordered by (expert, token) exactly,
 //     without any order decided by atomics;
 //  4. the work list of the expert kernels: groups of at most GN rows of one expert
-//     (shared-expert groups first, over the tokens in order), each with its first row in
+//     (shared-expert groups first, over the tokens in order; only the experts of the
+//     call's share, see WsLayout), each with its first row in
 //     the tensor-core activation tiles (row index + 7 x group index: room to pad each
 //     group's rows to a multiple of 8).
 #include "dev.cuh"
@@ -21,7 +22,8 @@ namespace moe {
 
 // shared memory: masks [32][E] u32 | chunk bases [n_chunks][E] u16 | 2 x [E+1] int
 __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int n_shared, int GN,
-                                                       int P, const int32_t *ids,
+                                                       int P, int e0, int e1, int sh_on,
+                                                       const int32_t *ids,
                                                        int32_t *offsets_out, int32_t *perm,
                                                        int32_t *slot_pos, Group *groups,
                                                        Ctrl *ctrl) {
@@ -57,8 +59,9 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
       cbase[c * E + e] = (uint16_t)run;
       run += v;
     }
-    offs[e] = run;                    // counts for now
-    gstart[e] = (run + GN - 1) / GN;  // groups of this expert
+    offs[e] = run;  // counts for now
+    // groups of this expert (none for an expert outside the call's share)
+    gstart[e] = e >= e0 && e < e1 ? (run + GN - 1) / GN : 0;
   }
   __syncthreads();
   // 2b. exclusive scans of the per-expert counts and group counts (one warp, E <= 256)
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
       for (int q = 0; q < 2; q++) arr[q][E] = inc[q];
   }
   __syncthreads();
-  const int ns = n_shared ? (T + GN - 1) / GN : 0;
+  const int ns = n_shared && sh_on ? (T + GN - 1) / GN : 0;
   const int rbase = n_shared ? T : 0;  // routed rows follow the shared expert's T rows
   if (threadIdx.x == 0) ctrl->n_groups = ns + gstart[E];
   for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets_out[e] = offs[e];
@@ -120,7 +123,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
         }
         int pos = offs[e] + cbase[c * E + e] + __popc(my[e] & below);
         perm[pos] = t * k + j;
-        slot_pos[t * k + j] = pos;
+        // a slot of an expert outside the call's share has no output row to combine
+        slot_pos[t * k + j] = e >= e0 && e < e1 ? pos : -1;
       }
     }
     __syncwarp();
@@ -128,7 +132,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, int 
   // 4. groups
   for (int i = threadIdx.x; i < ns; i += blockDim.x)
     groups[i] = Group{E, i * GN, min(GN, T - i * GN), P * i * GN + 7 * i, i * GN + 7 * i, 0, 0, 0};
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
     int n = offs[e + 1] - offs[e];
     int g0 = ns + gstart[e];
     for (int g = 0; g * GN < n; g++)
@@ -151,7 +155,8 @@ int launch_permute(const moe_layer_config &c, int T, const int32_t *ids, uint8_t
   if (smem > 48 * 1024)
     set_dyn_smem((const void *)permute_kernel, (int)smem);
   if (launch_pdl(permute_kernel, dim3(1), dim3(1024), smem, st, T, c.top_k, c.n_experts,
-                 c.n_shared, W.group_n, W.pieces, ids, (int32_t *)(ws + W.offsets),
+                 c.n_shared, W.group_n, W.pieces, W.e0, W.e1, W.shared ? 1 : 0, ids,
+                 (int32_t *)(ws + W.offsets),
                  (int32_t *)(ws + W.perm), (int32_t *)(ws + W.slot_pos), (Group *)(ws + W.groups),
                  (Ctrl *)(ws + W.ctrl)) != cudaSuccess)
     return MOE_ERR_CUDA;

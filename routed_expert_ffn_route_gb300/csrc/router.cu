@@ -67,6 +67,7 @@ struct FrontArgs {
   uint8_t *xt;
   float *rscale;
   int P, GN;
+  int e0, e1, shared;  // the call's share: routed experts [e0, e1), the shared expert
   long long *trace;  // development builds: phase times of the fused front
 };
 
@@ -522,13 +523,14 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
   // exclusive scans over the experts (thread e): slot offsets and group numbers
   const uint32_t m = tid < E ? sm.emask[tid] : 0u;
   const int cnt = __popc(m);
+  const bool mine = tid >= f.e0 && tid < f.e1;  // the expert is in the call's share
   int inc = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, inc, o);
     if (lane >= o) inc += v;
   }
-  const unsigned used = __ballot_sync(0xffffffffu, cnt > 0);
+  const unsigned used = __ballot_sync(0xffffffffu, cnt > 0 && mine);
   if (lane == 31) sm.wsum[warp] = inc;
   if (lane == 0) sm.wused[warp] = __popc(used);
   __syncthreads();
@@ -541,7 +543,7 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
     gtotal += sm.wused[q];
     total += sm.wsum[q];
   }
-  const int ns = c.n_shared ? (T + GN - 1) / GN : 0;
+  const int ns = c.n_shared && f.shared ? (T + GN - 1) / GN : 0;
   const int rbase = c.n_shared ? T : 0;  // routed rows follow the shared expert's T rows
   const int ng = ns + gtotal;
   if (tid < E) {
@@ -550,7 +552,7 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
     f.offsets[tid] = off;
     const int g0 = ns + gbase + __popc(used & ((1u << lane) - 1u));
     sm.xrow0[tid] = P * (rbase + off) + 7 * g0;
-    if (cnt)
+    if (cnt && mine)
       f.groups[g0] = Group{tid, off, cnt, P * (rbase + off) + 7 * g0, rbase + off + 7 * g0,
                            0, 0, 0};
   }
@@ -570,9 +572,12 @@ __device__ void front_tail(const moe_layer_config &c, const FrontArgs &f, const 
     const int e = sm.ids[tid], t = tid / k;
     const int r = __popc(sm.emask[e] & ((1u << t) - 1u)), pos = sm.offs[e] + r;
     f.perm[pos] = tid;
-    f.slot_pos[tid] = pos;
+    // a slot of an expert outside the call's share has no group and no output row
+    const bool mine_e = e >= f.e0 && e < f.e1;
+    f.slot_pos[tid] = mine_e ? pos : -1;
     const float inv = 1.0f / sm.tscale[t];
-    for (int p = 0; p < P; p++) f.rscale[sm.xrow0[e] + P * r + p] = inv;
+    if (mine_e)
+      for (int p = 0; p < P; p++) f.rscale[sm.xrow0[e] + P * r + p] = inv;
   }
   // the shared expert's rows: token t is row t of group t / GN
   for (int i = tid; i < (ns ? T : 0); i += blockDim.x) {
@@ -778,6 +783,9 @@ int launch_router(const moe_layer_config &c, const uint8_t *packed, const void *
       f.rscale = (float *)(ws + W.rscale);
       f.P = W.pieces;
       f.GN = W.group_n;
+      f.e0 = W.e0;
+      f.e1 = W.e1;
+      f.shared = W.shared ? 1 : 0;
 #ifdef MOE_TRACE
       f.trace = g_router_trace;
 #endif

@@ -99,3 +99,70 @@ def make_experts_fast(spec, seed, layer, which) -> dict:
                                s_up=gen.expert_scales(spec, seed, layer, e, "up"),
                                s_down=gen.expert_scales(spec, seed, layer, e, "down"))
     return out
+
+
+def _masked(ids, keep):
+    """ids with every slot whose expert is not in `keep` dropped (id -1)."""
+    return np.where(np.isin(ids, list(keep)), ids, -1).astype(np.int32)
+
+
+def oracle_out_many(spec, L: GpuLayer, x, ids, w, tokens, chunk=32, threads=None,
+                    in_flight=24):
+    """fp64 oracle output for many tokens of a large layer, in bounded host memory.
+
+    The layer output is a sum over slots (out[t] = shared(x_t) + sum_j w[t][j] y_j), so it
+    is computed as independent partial layers that the oracle evaluates, each on a chunk of
+    at most `chunk` tokens: one routed expert at a time (the token's other slots dropped,
+    id -1, no shared expert), plus the shared expert alone.  The partials run in a thread
+    pool (the oracle releases the interpreter while it computes) and are summed in fp64;
+    experts are drawn (on the device, bit-identical to the host stream) as they are
+    needed, at most `in_flight` at a time."""
+    import concurrent.futures as cf
+    import os
+    tok = np.asarray(tokens)
+    x64 = x[tok].astype(np.float64)
+    ids_t, w_t = ids[tok], w[tok]
+    out = np.zeros((len(tok), spec.hidden), dtype=np.float64)
+    threads = threads or max(1, min(16, os.cpu_count() or 1))
+    routed_only = spec.replace(n_shared=0)
+
+    def run(sp, rows, ids_m, ex, sh):
+        return rows, oracle.layer_experts(sp, x64[rows], ids_m, w_t[rows], ex, sh, mode=1)
+
+    with cf.ThreadPoolExecutor(threads) as pool:
+        pending = []
+
+        def drain(limit):
+            while len(pending) > limit:
+                rows, part = pending.pop(0).result()
+                out[rows] += part
+
+        if spec.n_shared:
+            sh = make_experts_fast(spec, L.seed, L.layer, [spec.n_experts])[spec.n_experts]
+            none = np.full_like(ids_t, -1)
+            for s0 in range(0, len(tok), chunk):
+                rows = np.arange(s0, min(len(tok), s0 + chunk))
+                pending.append(pool.submit(run, spec, rows, none[rows], {}, sh))
+        for e in sorted(set(int(v) for v in ids_t.ravel() if v >= 0)):
+            ex = make_experts_fast(spec, L.seed, L.layer, [e])
+            users = np.nonzero((ids_t == e).any(1))[0]
+            for s0 in range(0, len(users), chunk):
+                rows = users[s0:s0 + chunk]
+                pending.append(pool.submit(run, routed_only, rows, _masked(ids_t[rows], {e}),
+                                           ex, None))
+            drain(in_flight)
+        drain(0)
+    return out
+
+
+def prefill_sample(ids, n_experts, busiest=3, spread=32):
+    """Tokens whose outputs a full-size prefill check compares: every token routed to the
+    `busiest` most-loaded experts (each of their groups, so every m-tile of a group and
+    both groups of an expert split in two), plus `spread` tokens evenly over the batch
+    (one in every group of the shared expert)."""
+    T = ids.shape[0]
+    load = np.bincount(ids[ids >= 0].ravel(), minlength=n_experts)
+    top = np.argsort(-load, kind="stable")[:busiest]
+    users = np.nonzero(np.isin(ids, top).any(1))[0]
+    even = np.unique(np.linspace(0, T - 1, spread).round().astype(int))
+    return np.union1d(users, even), top, load[top]

@@ -164,3 +164,16 @@ def test_top_p_validation(L):
                   (float("inf"), False)):
         cfg.expert_top_p = p
         assert (moe.moe_check_config(cfg) == moe.MOE_OK) == ok, p
+
+
+def test_expert_share_arguments_rejected_before_any_launch(L):
+    cfg = config_for(gen.spec("dsv3"))
+    P = C.c_void_p
+    call = lambda b, e, sh, T=4: L.moe_layer_forward_experts(
+        C.byref(cfg), P(256), P(256), moe.MOE_DT_BF16, T, b, e, sh, P(256), P(256), P(256),
+        P(256), 1 << 40, None)
+    for b, e, sh in [(-1, 4, 0), (5, 4, 0), (0, 257, 1), (0, 256, 2), (0, 256, -1)]:
+        assert call(b, e, sh) == moe.MOE_ERR_INVALID_ARG, (b, e, sh)
+    # an empty share is valid (its output is the shared expert, or zero); T == 0 is a no-op
+    assert call(3, 3, 0, T=0) == moe.MOE_OK
+    assert call(0, 256, 1, T=0) == moe.MOE_OK

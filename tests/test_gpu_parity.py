@@ -14,7 +14,7 @@ import gen
 import gen.device
 import oracle
 import routed_expert_ffn_route_gb300 as moe
-from _gpu_support import GpuLayer, get_layer, inputs, oracle_out
+from _gpu_support import GpuLayer, get_layer, inputs, oracle_out, oracle_out_many, prefill_sample
 from _support import FROB_REL, MAX_REL_RMS, err_stats
 
 pytestmark = pytest.mark.gpu
@@ -40,6 +40,10 @@ def assert_close(got, ref, what):
 
 
 def check_layer(spec, T, batch=0, sample=None, seed=0):
+    """The layer forward against the oracle: ids, weights and the permutation on every
+    token; the output on every token (sample None), on `sample` tokens spread over the
+    batch (an int), or (sample "prefill") on every token of the three most-loaded experts
+    plus 32 spread tokens."""
     L = get_layer(spec, seed)
     x, xd, ids_o, w_o, margin, redraws = inputs(spec, L, batch, T)
     out, ids, w = L.forward(xd)
@@ -51,9 +55,18 @@ def check_layer(spec, T, batch=0, sample=None, seed=0):
     off_o, perm_o = oracle.permutation(ids_o, spec.n_experts)
     off_g, perm_g = L.permutation(T)
     assert np.array_equal(off_g, off_o) and np.array_equal(perm_g, perm_o)
-    tok = None if sample is None else np.unique(
-        np.linspace(0, T - 1, sample).round().astype(int))
-    ref = oracle_out(spec, L, x, ids_o, w_o, tok)
+    if sample == "prefill":
+        tok, top, load = prefill_sample(ids_o, spec.n_experts)
+        print(f"{spec.name} T={T}: output compared on {len(tok)} tokens (experts {top.tolist()} "
+              f"with {load.tolist()} tokens, and 32 spread)")
+    else:
+        tok = None if sample is None else np.unique(
+            np.linspace(0, T - 1, sample).round().astype(int))
+    n = T if tok is None else len(tok)
+    if n * (spec.top_k + spec.n_shared) * spec.hidden * spec.inter > 4e9:
+        ref = oracle_out_many(spec, L, x, ids_o, w_o, np.arange(T) if tok is None else tok)
+    else:
+        ref = oracle_out(spec, L, x, ids_o, w_o, tok)
     got = out_g if tok is None else out_g[tok]
     assert_close(got, ref, f"{spec.name} T={T} output")
     return out, ids, w, xd, L
@@ -75,6 +88,46 @@ def test_pack_unpack_bit_identity(bits):
         for w in rows:
             assert np.array_equal(outs[w].cpu().numpy(), gen.expert_codes(s, 3, 0, e, w))
             assert np.array_equal(sc[w].cpu().numpy(), gen.expert_scales(s, 3, 0, e, w))
+
+
+@pytest.mark.parametrize("bits", [4, 8, 2])
+def test_pack_weights_matches_incremental_packing(bits):
+    # moe_pack_weights takes every expert's containers stacked ([E][I][H] ...) in one call;
+    # the blob must be byte-identical to the one moe_pack_router + moe_pack_expert write
+    s = small("grouped", weight_bits=bits)
+    seed = 13
+    cfg = gen.device.config_for(s)
+    n = moe.moe_packed_bytes(cfg)
+    inc = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    gen.device.build_packed_layer(s, seed, 0, "cuda", packed=inc, host_codes=True)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    stack = lambda which: dev(np.stack([gen.expert_codes(s, seed, 0, e, which)
+                                        for e in range(s.n_experts)]))
+    sstack = lambda which: dev(np.stack([gen.expert_scales(s, seed, 0, e, which)
+                                         for e in range(s.n_experts)]))
+    E = s.n_experts
+    src = {"gate": stack("gate"), "up": stack("up"), "down": stack("down"),
+           "s_gate": sstack("gate"), "s_up": sstack("up"), "s_down": sstack("down"),
+           "sh_gate": dev(gen.expert_codes(s, seed, 0, E, "gate")),
+           "sh_up": dev(gen.expert_codes(s, seed, 0, E, "up")),
+           "sh_down": dev(gen.expert_codes(s, seed, 0, E, "down")),
+           "sh_s_gate": dev(gen.expert_scales(s, seed, 0, E, "gate")),
+           "sh_s_up": dev(gen.expert_scales(s, seed, 0, E, "up")),
+           "sh_s_down": dev(gen.expert_scales(s, seed, 0, E, "down")),
+           "router_w": dev(gen.router_weights(s, seed, 0)),
+           "router_bias": dev(gen.router_bias(s, seed, 0).astype(np.float32))}
+    one = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    moe.moe_pack_weights(cfg, src, one)
+    torch.cuda.synchronize()
+    assert torch.equal(one, inc)
+    # and the packed layer computes the oracle's layer
+    L = GpuLayer.__new__(GpuLayer)
+    L.spec, L.seed, L.layer, L.cfg, L.packed = s, seed, 0, cfg, one
+    L.wr, L.bias, L._ws = gen.router_weights(s, seed, 0), gen.router_bias(s, seed, 0), {}
+    x, xd, ids_o, w_o, *_ = inputs(s, L, 0, 9)
+    out, ids, w = L.forward(xd)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert_close(out.cpu().numpy(), oracle_out(s, L, x, ids_o, w_o), f"packed in one call, {bits}-bit")
 
 
 def test_pack_unpack_full_size_expert():
@@ -129,6 +182,21 @@ def test_layer_tiny_full():
 @pytest.mark.parametrize("T", [1, 2, 7, 33, 37, 64])
 def test_layer_small_grouped_ragged(T):
     check_layer(small("grouped"), T, seed=1)
+
+
+@pytest.mark.parametrize("x_dtype,T", [("bf16", 300), ("f32", 150)])
+def test_layer_small_large_groups(x_dtype, T):
+    # four experts, two per token: groups of more than 64 activation rows take the
+    # tensor-core kernel's widest tile (128 rows), experts with more than 128 rows split
+    # into two groups, and the shared expert's tokens fill several 128-row groups; every
+    # element is compared
+    s = small("softmax", n_experts=4, top_k=2, n_shared=1, inter_shared=256, x_dtype=x_dtype)
+    L = get_layer(s, 11)
+    x, xd, ids_o, *_ = inputs(s, L, 0, T)
+    rows = np.bincount(ids_o.ravel(), minlength=4) * (2 if x_dtype == "f32" else 1)
+    print(f"activation rows per expert: {rows.tolist()}")
+    assert rows.max() > 128
+    check_layer(s, T, seed=11)
 
 
 @pytest.mark.parametrize("bits", [8, 2])
@@ -194,11 +262,14 @@ def test_layer_deterministic_and_T0_noop():
     moe.moe_layer_forward(L.cfg, L.packed, empty, out, ids, w, L.ws(1))
 
 
-# full-size layers (the benchmark's shapes); large T checks sampled tokens
+# full-size layers (the benchmark's shapes): every token up to T = 64; at prefill sizes
+# every token of the three most-loaded experts (their groups cover every m-tile of the
+# tensor-core kernel, and an expert with more than 128 tokens forms two groups) plus 32
+# spread tokens (one in every group of the shared expert)
 @pytest.mark.parametrize("name,T,sample", [("mixtral", 1, None), ("dsv3", 1, None),
-                                           ("dsv3", 16, 3), ("dsv3", 2048, 2),
-                                           ("dsv3_int2", 1, None), ("dsv3_int8", 4, 2),
-                                           ("dsv3_int8", 64, 2), ("mixtral", 512, 2)])
+                                           ("dsv3", 16, None), ("dsv3", 2048, "prefill"),
+                                           ("dsv3_int2", 1, None), ("dsv3_int8", 4, None),
+                                           ("dsv3_int8", 64, None), ("mixtral", 512, "prefill")])
 def test_layer_full_size(name, T, sample):
     check_layer(gen.spec(name), T, sample=sample)
 

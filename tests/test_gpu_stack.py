@@ -20,7 +20,7 @@ import routed_expert_ffn_route_gb300 as moe
 from routed_expert_ffn_route_gb300.stack import Stack
 from gen.device import build_packed_layer, hidden_to_device
 from _support import FROB_REL, MAX_REL_RMS, err_stats
-from _gpu_support import make_experts_fast
+from _gpu_support import make_experts_fast, oracle_out_many
 
 pytestmark = pytest.mark.gpu
 
@@ -182,3 +182,48 @@ def test_c5_gpu_stack(c5):
         r1 = st.forward(hidden_to_device(SPEC, xd, bd))
         st.status()
         assert torch.isfinite(r1).all()
+
+
+def test_c5_gpu_stack_end_to_end(c5):
+    """Stack.forward (every layer and stack step on the GPU, chained through the C ABI)
+    against the oracle's fp64 stack from the same input, on sampled rows of the T = 4096
+    prefill batch.
+
+    Rows are compared where the GPU selected the same experts as the oracle at every layer
+    (as sets: two selected experts whose scores are closer than the GPU's rounding may
+    swap slots, which only reorders the combine's sum).  The bar is the layer's bar
+    widened for the stack: each layer's input is re-rounded to bf16 (8 significant bits),
+    so the GPU's fp32 residual (relative error ~2e-4 per layer, the fp16 rounding of h)
+    makes a few percent of those roundings fall the other way (one bf16 unit, 2^-8
+    relative, each); through the quadratic SwiGLU that is a ~3e-3 relative change of each
+    later layer's output.  Final residual: relative Frobenius <= 1e-2, max|err| <= 5e-2 RMS."""
+    from types import SimpleNamespace
+    T = T_PREFILL
+    st = Stack(c5, T, eps=EPS)
+    x, bits = gen.hidden_states(SPEC, SEED, 62, T)
+    r_gpu = st.forward(hidden_to_device(SPEC, x, bits))
+    st.status()
+    rows = np.unique(np.linspace(0, T - 1, 12).round().astype(int))
+    r_gpu = r_gpu.cpu().numpy()[rows].astype(np.float64)
+    ids_gpu = [st.ids[l][:T].cpu().numpy()[rows] for l in range(LAYERS)]
+    # the oracle's stack on those rows
+    r, xn = oracle.residual_rmsnorm(x[rows].astype(np.float64), None, eps=EPS)
+    same = np.ones(len(rows), dtype=bool)
+    min_margin = np.full(len(rows), np.inf)
+    for l in range(LAYERS):
+        wr = gen.router_weights(SPEC, SEED, l)
+        ids, w, margin = oracle.route(SPEC, oracle.router_logits(SPEC, xn, wr), bias(l))
+        min_margin = np.minimum(min_margin, margin)
+        same &= np.array([np.array_equal(np.sort(a), np.sort(b)) for a, b in zip(ids, ids_gpu[l])])
+        out = oracle_out_many(SPEC, SimpleNamespace(seed=SEED, layer=l), xn, ids, w,
+                              np.arange(len(rows)))
+        r, xn = oracle.residual_rmsnorm(r, out, eps=EPS)
+    print(f"rows {rows.tolist()}: same experts at every layer {same.tolist()}, "
+          f"min oracle margin {np.round(min_margin, 5).tolist()}")
+    # a row whose every decision is far from a tie must route alike on the GPU
+    assert same[min_margin >= 2e-3].all()
+    assert same.sum() >= len(rows) // 2
+    mx, fr = err_stats(r_gpu[same], r[same])
+    print(f"final residual after {LAYERS} layers ({same.sum()} rows): max|err|/RMS = {mx:.2e}, "
+          f"rel Frobenius = {fr:.2e}")
+    assert fr <= 1e-2 and mx <= 5e-2

@@ -5,9 +5,11 @@ receives its input and output tensors, a serving loop that forbids allocation af
 start-up, code that must not call cudaMalloc because it may synchronise the device), the
 library keeps its scratch in its own 32 MiB device array.  This test calls that entry
 point through the C ABI twice in a row and checks each result against moe_layer_forward
-with a caller workspace, within the parity tolerance of the other tests.  It builds its
-own layer, so it passes alone in a fresh process as well as after the other tests; the
-file name makes pytest collect it last.
+with a caller workspace: the same kernels on the same inputs, so ids, weights and output
+must be bit-identical; the first call is also checked against the fp64 oracle within the
+parity tolerance of the other tests.  It builds its own layer, so it passes alone in a
+fresh process as well as after the other tests; the file name makes pytest collect it
+last.
 """
 import ctypes as C
 
@@ -18,10 +20,12 @@ import torch
 import gen
 import gen.device
 import routed_expert_ffn_route_gb300 as moe
-from _gpu_support import GpuLayer, inputs
+from _gpu_support import GpuLayer, inputs, oracle_out, oracle_out_many
 from _support import FROB_REL, MAX_REL_RMS, err_stats
 
 pytestmark = pytest.mark.gpu
+
+STATIC_BYTES = 32 << 20  # the library's scratch array
 
 
 def _call_static(L, xd, T):
@@ -41,31 +45,50 @@ def _call_static(L, xd, T):
     return out, ids, w
 
 
-@pytest.mark.parametrize("spec,T", [
-    (gen.LayerSpec("noalloc_small", hidden=512, inter=384, n_experts=16, top_k=4,
-                   router="sigmoid_grouped", n_shared=1, inter_shared=256, n_group=4,
-                   topk_group=2, rsf=2.5, bias_std=0.1), 37),
-    (gen.spec("dsv3"), 16),
-])
+def _largest_static_T(cfg):
+    """The largest T whose workspace fits the static array (the entry point's limit)."""
+    T = 1
+    while moe.moe_workspace_bytes(cfg, T + 1) <= STATIC_BYTES:
+        T += 1
+    return T
+
+
+SMALL = gen.LayerSpec("noalloc_small", hidden=512, inter=384, n_experts=16, top_k=4,
+                      router="sigmoid_grouped", n_shared=1, inter_shared=256, n_group=4,
+                      topk_group=2, rsf=2.5, bias_std=0.1)
+
+
+@pytest.mark.parametrize("spec,T", [(SMALL, 37), (gen.spec("dsv3"), 16),
+                                    (gen.spec("dsv3"), "largest")])
 def test_static_scratch_forward_matches_workspace_forward(spec, T):
     L = GpuLayer(spec, seed=21)
-    _, xd, *_ = inputs(spec, L, 5, T)
-    ref_out, ref_ids, ref_w = L.forward(xd)
-    ref_out, ref_ids, ref_w = ref_out.cpu().numpy(), ref_ids.cpu().numpy(), ref_w.cpu().numpy()
-    for _ in range(2):  # two calls in a row share (and reuse) the static array
-        out, ids, w = _call_static(L, xd, T)
-        assert np.array_equal(ids.cpu().numpy(), ref_ids)
-        for got, ref in ((out.cpu().numpy(), ref_out), (w.cpu().numpy(), ref_w)):
-            mx, fr = err_stats(got, ref)
-            assert mx <= MAX_REL_RMS and fr <= FROB_REL, (mx, fr)
+    if T == "largest":
+        T = _largest_static_T(L.cfg)
+        print(f"{spec.name}: largest T for the static scratch = {T}")
+    x, xd, ids_o, w_o, *_ = inputs(spec, L, 5, T)
+    ref = [t.clone() for t in L.forward(xd)]
+    for call in range(2):  # two calls in a row share (and reuse) the static array
+        got = _call_static(L, xd, T)
+        for g, r, what in zip(got, ref, ("out", "ids", "w")):
+            assert torch.equal(g, r), f"call {call}: {what} differs from the workspace forward"
+    assert np.array_equal(ref[1].cpu().numpy(), ids_o)
+    many = T * (spec.top_k + spec.n_shared) * spec.hidden * spec.inter > 4e9
+    want = (oracle_out_many(spec, L, x, ids_o, w_o, np.arange(T)) if many
+            else oracle_out(spec, L, x, ids_o, w_o))
+    mx, fr = err_stats(ref[0].cpu().numpy(), want)
+    print(f"{spec.name} T={T} static forward vs oracle: max|err|/RMS = {mx:.2e}, "
+          f"rel Frobenius = {fr:.2e}")
+    assert mx <= MAX_REL_RMS and fr <= FROB_REL
 
 
 def test_static_scratch_rejects_oversized_calls():
     s = gen.spec("dsv3")
     cfg = gen.device.config_for(s)
-    T = 64  # its workspace is far above the 32 MiB array
-    assert moe.moe_workspace_bytes(cfg, T) > (32 << 20)
-    r = moe.lib().moe_layer_forward_static(
-        C.byref(cfg), C.c_void_p(256), C.c_void_p(256), moe.MOE_DT_BF16, T, C.c_void_p(256),
-        C.c_void_p(256), C.c_void_p(256), None, None)
-    assert r == moe.MOE_ERR_WORKSPACE
+    largest = _largest_static_T(cfg)
+    assert moe.moe_workspace_bytes(cfg, largest) <= STATIC_BYTES
+    for T in (largest + 1, 64):  # the first size whose workspace exceeds the array, and more
+        assert moe.moe_workspace_bytes(cfg, T) > STATIC_BYTES
+        r = moe.lib().moe_layer_forward_static(
+            C.byref(cfg), C.c_void_p(256), C.c_void_p(256), moe.MOE_DT_BF16, T, C.c_void_p(256),
+            C.c_void_p(256), C.c_void_p(256), None, None)
+        assert r == moe.MOE_ERR_WORKSPACE
