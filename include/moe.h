@@ -176,6 +176,19 @@ int moe_layer_forward_experts(const moe_layer_config *cfg, const void *packed, c
                               int with_shared, float *out, int32_t *ids, float *w, void *ws,
                               size_t ws_bytes, void *stream);
 
+/* moe_layer_forward for one layer of a stack of layers ("colibrì 深度拆解" §4.3: a layer's
+ * merged output feeds the next layer; "Show HN: 如何在我的低配置电脑上运行 GLM-5.2", 已实现的功能:
+ * 异步专家预读, the next weights are read ahead while the current ones are in use): the same
+ * forward, whose last kernel (the combine) also starts loading the NEXT layer's router
+ * weights and bias (next_cfg, next_packed: that layer's config and packed blob, device,
+ * 256-byte aligned) into L2, so that the next layer's router finds them there.  A hint: the
+ * results are those of moe_layer_forward, bit for bit.  next_cfg / next_packed NULL or an
+ * unsupported next_cfg: MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED before any launch. */
+int moe_layer_forward_next(const moe_layer_config *cfg, const void *packed, const void *x,
+                           moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
+                           size_t ws_bytes, const moe_layer_config *next_cfg,
+                           const void *next_packed, void *stream);
+
 /* moe_layer_forward with stage timing: records the caller's CUDA events (cudaEvent_t
  * passed as void*) on `stream` around the stages, events[0] before the first kernel and
  * events[i+1] after stage i, for the stages 0 router (logits + top-k), 1 permutation,

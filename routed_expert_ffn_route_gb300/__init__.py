@@ -18,7 +18,7 @@ __all__ = [
     "moe_workspace_bytes", "moe_pack_weights", "moe_pack_router", "moe_pack_expert",
     "moe_unpack_weights", "moe_route_topk", "moe_layer_forward", "moe_read_status",
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
-    "moe_debug_wait_timeout", "moe_layer_forward_experts", "EXPORTED",
+    "moe_debug_wait_timeout", "moe_layer_forward_experts", "moe_layer_forward_next", "EXPORTED",
     "MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED", "MOE_ERR_WORKSPACE",
     "MOE_ERR_CUDA", "MOE_ERR_TIMEOUT", "MOE_ERR_NUMERIC", "MOE_ERR_PACKED",
 ]
@@ -39,7 +39,7 @@ EXPORTED = [
     "moe_debug_permutation", "moe_q8_0_quantize", "moe_debug_block_dots",
     "moe_debug_wait_timeout", "moe_layer_forward_timed", "moe_forward_launches",
     "moe_layer_forward_static", "moe_residual_rmsnorm", "moe_quantize_rows",
-    "moe_layer_forward_experts",
+    "moe_layer_forward_experts", "moe_layer_forward_next",
 ]
 
 # stages bracketed by the events of moe_layer_forward_timed
@@ -114,6 +114,7 @@ def _bind(L):
         "moe_residual_rmsnorm": (I, [I, I, P, P, P, C.c_float, P, P]),
         "moe_quantize_rows": (I, [P, I, I, I, I, P, P, P]),
         "moe_layer_forward_experts": (I, [P, P, P, I, I, I, I, I, P, P, P, P, S, P]),
+        "moe_layer_forward_next": (I, [P, P, P, I, I, P, P, P, P, S, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -228,6 +229,14 @@ def moe_layer_forward_experts(cfg, packed, x, expert_begin, expert_end, with_sha
                                         int(expert_begin), int(expert_end), int(with_shared),
                                         _p(out), _p(ids), _p(w), _p(ws), ws.numel(),
                                         _stream(stream)), "moe_layer_forward_experts")
+
+
+def moe_layer_forward_next(cfg, packed, x, out, ids, w, ws, next_cfg, next_packed, stream=None):
+    """moe_layer_forward that also warms the next stacked layer's router weights into L2."""
+    T = x.shape[0]
+    _ck(lib().moe_layer_forward_next(C.byref(cfg), _p(packed), _p(x), _dtype(x), T, _p(out),
+                                     _p(ids), _p(w), _p(ws), ws.numel(), C.byref(next_cfg),
+                                     _p(next_packed), _stream(stream)), "moe_layer_forward_next")
 
 
 def moe_layer_forward_timed(cfg, packed, x, out, ids, w, ws, events, stream=None):

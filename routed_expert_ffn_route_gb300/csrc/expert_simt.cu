@@ -20,6 +20,7 @@
 // without an output row (dropped by top-p, or outside an expert-parallel share) are skipped.
 #include "dev.cuh"
 #include "moe_internal.cuh"
+#include "tc.cuh"
 
 namespace moe {
 
@@ -260,8 +261,20 @@ __global__ void __launch_bounds__(256) down_kernel(ExpertArgs a, int item_bound)
 }
 
 // ---------------------------------------------------------------- combine
+// pf, pf_bytes (may be null / 0): a region to start loading into L2 (the next stacked layer's
+// router weights), 32 KB slices spread over the threads of the first warp of every block;
+// issued before the wait, it depends on nothing this launch reads.
 __global__ void combine_kernel(int T, int H, int k, int n_shared, const float *w,
-                               const int32_t *slot_pos, const float *y, float *out) {
+                               const int32_t *slot_pos, const float *y, float *out,
+                               const uint8_t *pf, uint64_t pf_bytes) {
+  if (pf && threadIdx.x < 32) {
+    constexpr uint64_t kSlice = 32 * 1024;
+    for (uint64_t off = ((uint64_t)blockIdx.x * 32 + threadIdx.x) * kSlice; off < pf_bytes;
+         off += (uint64_t)gridDim.x * 32 * kSlice) {
+      const uint64_t n = pf_bytes - off < kSlice ? pf_bytes - off : kSlice;
+      tc::bulk_prefetch_l2(pf + off, (uint32_t)n);
+    }
+  }
   pdl_wait();
   pdl_trigger();
   long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -375,11 +388,11 @@ int launch_quant_x(const moe_layer_config &c, const void *x, moe_dtype dt, int T
 }
 
 int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
-                   const WsLayout &W, cudaStream_t st) {
+                   const WsLayout &W, cudaStream_t st, const uint8_t *pf, uint64_t pf_bytes) {
   long n = (long)T * (c.hidden / 4);
   if (launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, T, c.hidden,
                  c.top_k, c.n_shared && W.shared ? 1 : 0, w, (const int32_t *)(ws + W.slot_pos),
-                 (const float *)(ws + W.y), out) != cudaSuccess)
+                 (const float *)(ws + W.y), out, pf, pf_bytes) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

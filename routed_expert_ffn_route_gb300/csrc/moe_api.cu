@@ -264,7 +264,8 @@ int moe_route_topk(const moe_layer_config *cfg, const void *packed, const void *
 static int forward_impl(const moe_layer_config *cfg, const void *packed, const void *x,
                         moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
                         size_t ws_bytes, void *const *ev, void *stream,
-                        const int *share = nullptr) {
+                        const int *share = nullptr, const uint8_t *pf = nullptr,
+                        uint64_t pf_bytes = 0) {
   WsLayout W;
   int r = common_args(cfg, packed, x, dtype, T, ids, w, ws, ws_bytes, &W);
   if (r || T == 0) return r;
@@ -294,7 +295,7 @@ static int forward_impl(const moe_layer_config *cfg, const void *packed, const v
                           ev ? ev[4] : nullptr, fused)))
     return r;
   if (!mark(5)) return MOE_ERR_CUDA;
-  if ((r = launch_combine(*cfg, T, w, out, wsb, W, st))) return r;
+  if ((r = launch_combine(*cfg, T, w, out, wsb, W, st, pf, pf_bytes))) return r;
   return mark(6) ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -316,6 +317,23 @@ int moe_layer_forward_experts(const moe_layer_config *cfg, const void *packed, c
   const int share[3] = {expert_begin, expert_end, with_shared};
   return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, nullptr, stream,
                       share);
+}
+
+int moe_layer_forward_next(const moe_layer_config *cfg, const void *packed, const void *x,
+                           moe_dtype dtype, int T, float *out, int32_t *ids, float *w, void *ws,
+                           size_t ws_bytes, const moe_layer_config *next_cfg,
+                           const void *next_packed, void *stream) {
+  int r = check(cfg);
+  if (r) return r;
+  if (!next_cfg || !next_packed) return MOE_ERR_INVALID_ARG;
+  if ((r = check(next_cfg))) return r;
+  if (!aligned(next_packed, 256)) return MOE_ERR_INVALID_ARG;
+  // the next layer's router weights and bias (contiguous in its blob)
+  const PackLayout P = pack_layout(*next_cfg);
+  const uint64_t bytes = align_up((uint64_t)next_cfg->n_experts * 4, 16) +
+                         (P.router_b_off - P.router_w_off);
+  return forward_impl(cfg, packed, x, dtype, T, out, ids, w, ws, ws_bytes, nullptr, stream, nullptr,
+                      (const uint8_t *)next_packed + P.router_w_off, bytes);
 }
 
 int moe_layer_forward_timed(const moe_layer_config *cfg, const void *packed, const void *x,

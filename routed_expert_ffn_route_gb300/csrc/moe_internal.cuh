@@ -275,8 +275,11 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
 int launch_experts(const moe_layer_config &c, const uint8_t *packed, const void *x,
                    moe_dtype dt, int T, uint8_t *ws, const WsLayout &W, cudaStream_t st,
                    void *act_event, void *mid_event, bool front_rows = false);
+// pf, pf_bytes: an optional region (16-byte aligned, a multiple of 16 bytes) the combine starts
+// loading into L2, for the launch that follows
 int launch_combine(const moe_layer_config &c, int T, const float *w, float *out, uint8_t *ws,
-                   const WsLayout &W, cudaStream_t st);
+                   const WsLayout &W, cudaStream_t st, const uint8_t *pf = nullptr,
+                   uint64_t pf_bytes = 0);
 int launch_pack_expert(const moe_layer_config &c, const ExpertLayout &L, const int8_t *gate,
                        const int8_t *up, const int8_t *down, const float *sg, const float *su,
                        const float *sd, uint8_t *base, cudaStream_t st);

@@ -4,15 +4,16 @@ feeds the next layer).
 The stacking arithmetic is the library's reading (the pages leave it open): the stack
 keeps an fp32 residual stream r; r_0 = x (the bf16 input), layer l runs on
 bf16(RMSNorm(r_l)) and r_{l+1} = r_l + MoE_l(...).  Every step runs in the library's
-kernels (`moe_layer_forward`, `moe_residual_rmsnorm`); this module only owns the buffers
-and issues the calls, so a whole prefill or decode step can be captured in one CUDA graph.
+kernels (`moe_layer_forward_next`, whose combine warms the next layer's router weights into
+L2, then `moe_residual_rmsnorm`); this module only owns the buffers and issues the calls, so
+a whole prefill or decode step can be captured in one CUDA graph.
 """
 from __future__ import annotations
 
 import torch
 
-from . import (moe_layer_forward, moe_read_status, moe_residual_rmsnorm, moe_workspace_bytes,
-               MOE_OK, MoEError)
+from . import (moe_layer_forward, moe_layer_forward_next, moe_read_status, moe_residual_rmsnorm,
+               moe_workspace_bytes, MOE_OK, MoEError)
 
 
 class Stack:
@@ -47,7 +48,12 @@ class Stack:
         r, x, out = self.resid[:T], self.x[:T], self.out[:T]
         moe_residual_rmsnorm(r, None, x, x0=x0, eps=self.eps)
         for l, (cfg, packed) in enumerate(self.layers):
-            moe_layer_forward(cfg, packed, x, out, self.ids[l][:T], self.w[l][:T], self.ws)
+            if l + 1 < len(self.layers):  # the combine warms the next layer's router into L2
+                ncfg, npacked = self.layers[l + 1]
+                moe_layer_forward_next(cfg, packed, x, out, self.ids[l][:T], self.w[l][:T],
+                                       self.ws, ncfg, npacked)
+            else:
+                moe_layer_forward(cfg, packed, x, out, self.ids[l][:T], self.w[l][:T], self.ws)
             moe_residual_rmsnorm(r, out, x, eps=self.eps)
         return r
 

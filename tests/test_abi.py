@@ -177,3 +177,17 @@ def test_expert_share_arguments_rejected_before_any_launch(L):
     # an empty share is valid (its output is the shared expert, or zero); T == 0 is a no-op
     assert call(3, 3, 0, T=0) == moe.MOE_OK
     assert call(0, 256, 1, T=0) == moe.MOE_OK
+
+
+def test_next_layer_forward_arguments_rejected_before_any_launch(L):
+    cfg = config_for(gen.spec("dsv3"))
+    bad = config_for(gen.spec("dsv3"))
+    bad.hidden = 100  # not a multiple of 128
+    P = C.c_void_p
+    call = lambda ncfg, npk, T=4: L.moe_layer_forward_next(
+        C.byref(cfg), P(256), P(256), moe.MOE_DT_BF16, T, P(256), P(256), P(256), P(256),
+        1 << 40, ncfg, npk, None)
+    assert call(None, P(256)) == moe.MOE_ERR_INVALID_ARG
+    assert call(C.byref(cfg), None) == moe.MOE_ERR_INVALID_ARG
+    assert call(C.byref(cfg), P(258)) == moe.MOE_ERR_INVALID_ARG
+    assert call(C.byref(bad), P(256)) == moe.MOE_ERR_UNSUPPORTED

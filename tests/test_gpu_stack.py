@@ -191,12 +191,11 @@ def test_c5_gpu_stack_end_to_end(c5):
 
     Rows are compared where the GPU selected the same experts as the oracle at every layer
     (as sets: two selected experts whose scores are closer than the GPU's rounding may
-    swap slots, which only reorders the combine's sum).  The bar is the layer's bar
-    widened for the stack: each layer's input is re-rounded to bf16 (8 significant bits),
-    so the GPU's fp32 residual (relative error ~2e-4 per layer, the fp16 rounding of h)
-    makes a few percent of those roundings fall the other way (one bf16 unit, 2^-8
-    relative, each); through the quadratic SwiGLU that is a ~3e-3 relative change of each
-    later layer's output.  Final residual: relative Frobenius <= 1e-2, max|err| <= 5e-2 RMS."""
+    swap slots, which only reorders the combine's sum).  The final residual is held to the
+    layer's own bar (max|err| <= 2e-3 RMS, relative Frobenius <= 1e-3): each layer's input
+    is re-rounded to bf16, and the GPU's fp32 residual can make a rounding fall the other
+    way, but the residual stream is dominated by the stack's input, so the 8-layer error
+    stays far inside that bar (measured ~5e-5 / ~1e-5)."""
     from types import SimpleNamespace
     T = T_PREFILL
     st = Stack(c5, T, eps=EPS)
@@ -226,4 +225,27 @@ def test_c5_gpu_stack_end_to_end(c5):
     mx, fr = err_stats(r_gpu[same], r[same])
     print(f"final residual after {LAYERS} layers ({same.sum()} rows): max|err|/RMS = {mx:.2e}, "
           f"rel Frobenius = {fr:.2e}")
-    assert fr <= 1e-2 and mx <= 5e-2
+    assert mx <= MAX_REL_RMS and fr <= FROB_REL
+
+
+def test_next_layer_forward_is_bit_identical(c5):
+    """moe_layer_forward_next (the combine also warms the next layer's router weights into
+    L2) returns exactly what moe_layer_forward returns, at decode and prefill sizes."""
+    (cfg, packed), (ncfg, npacked) = c5[0], c5[1]
+    for T in (1, 16, 300):
+        x, bits = gen.hidden_states(SPEC, SEED, 63, T)
+        xd = hidden_to_device(SPEC, x, bits)
+        ws = torch.zeros(moe.moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+        res = []
+        for nxt in (False, True):
+            out = torch.empty((T, SPEC.hidden), dtype=torch.float32, device="cuda")
+            ids = torch.empty((T, SPEC.top_k), dtype=torch.int32, device="cuda")
+            w = torch.empty((T, SPEC.top_k), dtype=torch.float32, device="cuda")
+            if nxt:
+                moe.moe_layer_forward_next(cfg, packed, xd, out, ids, w, ws, ncfg, npacked)
+            else:
+                moe.moe_layer_forward(cfg, packed, xd, out, ids, w, ws)
+            assert moe.moe_read_status(ws) == moe.MOE_OK
+            res.append((out, ids, w))
+        for a, b in zip(*res):
+            assert torch.equal(a, b)
