@@ -179,7 +179,7 @@ template <int BITS, bool DOWN, int NMAX>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int item_bound) {
   using PL = Plan<NMAX>;
   using RG = Rings<NMAX, BITS>;
-  constexpr int ST = PL::stages, NI = PL::issuers;
+  constexpr int NI = PL::issuers;
   constexpr int AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
   extern __shared__ uint8_t smraw[];
   uint8_t *base = tc::align_smem_1024(smraw);
@@ -193,6 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   const int a_run = ra * AB;                                  // bytes of a code run
   const int b_stride = (rb + (rb > 1 ? 1 : 0)) * NMAX * 128;  // run + the MMA's over-read
   const int SA = min(kMaxRuns, RG::a_ring / a_run), SB = min(kMaxRuns, RG::b_ring / b_stride);
+  // TMEM stages in use.  A dequantiser set waits only on the ring runs of its own units, so
+  // it may poll a ring stage for run r while run r - (ring size), one lap back, is still in
+  // flight; a parity wait cannot tell those two phases apart.  A set works at most ST units
+  // ahead of the oldest unit whose MMAs are unfinished, and every chunk before that window
+  // has landed, so the early pass cannot happen while the stages hold no more chunks than
+  // either ring: kUnit * ST <= SA * ra and <= SB * rb.
+  const int ST = min(PL::stages, min(SA * ra, SB * rb) / kUnit);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; s++) {
@@ -286,14 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
         if (!tc_item<DOWN>(a, item, it)) break;
-        // accumulator buffer n & 1, used for the (n >> 1)-th time
+        // accumulator buffer ab, used for the au-th time
+        const int ab = n % PL::acc_bufs, au = n / PL::acc_bufs;
         int got = 1;
-        if (leader) got = tc::mbar_wait(&bars->acc_empty[n & 1], ((n >> 1) & 1) ^ 1, abort, lim);
+        if (leader) got = tc::mbar_wait(&bars->acc_empty[ab], (au & 1) ^ 1, abort, lim);
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t idesc = tc::idesc_f16(0, it.Npad);  // fp16 x fp16 -> fp32
-        const uint32_t dcol = tbase + PL::acc_col + (n & 1) * NMAX;
+        const uint32_t dcol = tbase + PL::acc_col + ab * NMAX;
         for (int ku = 0; ku < it.KC; ku += kUnit, tpos.next(ST)) {
           got = 1;
           if (leader) MOE_TC_TRACE(10, c);
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
           issued = true;
         }
         if (!ok) break;
-        if (leader) tc::mma_commit(&bars->acc_full[n & 1]);
+        if (leader) tc::mma_commit(&bars->acc_full[ab]);
         __syncwarp();
       }
       if (!ok && leader) {
@@ -415,9 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     Item it;
     for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
       if (!tc_item<DOWN>(a, item, it)) break;
+      const int ab = n % PL::acc_bufs, au = n / PL::acc_bufs;
       ok = __all_sync(0xffffffffu,
-                      tc::mbar_wait_backoff(&bars->acc_full[n & 1], (n >> 1) & 1, abort, lim, 256));
-      d0 = tbase + tlane + PL::acc_col + (n & 1) * NI * NMAX;
+                      tc::mbar_wait_backoff(&bars->acc_full[ab], au & 1, abort, lim, 256));
+      d0 = tbase + tlane + PL::acc_col + ab * NI * NMAX;
       if (!ok) break;
       MOE_TC_TRACE_R(8, n);
       tc::fence_after_sync();
@@ -480,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       tc::fence_before_sync();
       __syncwarp();
       MOE_TC_TRACE_R(9, n);
-      if (lane == 0) tc::mbar_arrive(&bars->acc_empty[n & 1]);
+      if (lane == 0) tc::mbar_arrive(&bars->acc_empty[ab]);
     }
     if (!ok && lane == 0) give_up();
   }
