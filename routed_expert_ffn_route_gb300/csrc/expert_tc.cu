@@ -503,10 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
 // row] of fp16 x_t * tscale[t], row = token * P + piece (fp32 x is split into fp16 hi + lo
 // pieces); the padding rows are zero.  Also rscale[row] = 1 / tscale of the row's token.
 // One warp per tile row: it reads the token's x row front to back and, for each k-chunk,
-// eight lanes write the chunk's 128-byte line (16 bytes each, at its swizzled slot).
+// eight lanes write the chunk's 128-byte line (16 bytes each, at its swizzled slot).  The
+// tokens and scales of a warp's rows are looked up together first (a lane per row), so the
+// x loads of consecutive rows do not each wait behind two dependent lookups.
 // blockIdx.x: group; the warps of blockIdx.y stride over the group's rows.
-__global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, int is_bf16,
-                                                       const int32_t *perm, const float *tscale) {
+__global__ void __launch_bounds__(256, 5) gather_x_kernel(TcArgs a, const void *x, int is_bf16,
+                                                          const int32_t *perm, const float *tscale) {
   pdl_wait();
   pdl_trigger();
   const int gi = blockIdx.x;
@@ -520,47 +522,64 @@ __global__ void __launch_bounds__(256) gather_x_kernel(TcArgs a, const void *x, 
   // each taking every wpr-th group of four k-chunks
   const int W = gridDim.y * 8, wid = blockIdx.y * 8 + warp;
   const int wpr = W > rows8 ? W / rows8 : 1, part = wid % wpr;
-  for (int row = wid / wpr; row < rows8; row += W / wpr) {
-    const int c = lane & 7;  // the lane's 16-byte slot of a 128-byte line
-    if (row >= rows) {
-      for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr)
-        *(uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4)) =
-            make_uint4(0, 0, 0, 0);
-      if (lane == 0 && part == 0) a.rscale[g.xrow0 + row] = 0.f;
-      continue;
+  const int r0 = wid / wpr, rstep = W / wpr;
+  const int nr = rows8 > r0 ? (rows8 - r0 + rstep - 1) / rstep : 0;  // this warp's rows
+  const int c = lane & 7;  // the lane's 16-byte slot of a 128-byte line
+  for (int jb = 0; jb < nr; jb += 32) {
+    int ltok = 0;
+    float lsc = 0.f;
+    {
+      const int j = jb + lane, row = r0 + j * rstep;
+      if (j < nr && row < rows) {
+        const int i = row / a.P;
+        ltok = sh ? g.pos0 + i : perm[g.pos0 + i] / a.k;
+        lsc = tscale[ltok];
+        if (part == 0) a.rscale[g.xrow0 + row] = 1.0f / lsc;
+      } else if (j < nr && part == 0) {
+        a.rscale[g.xrow0 + row] = 0.f;
+      }
     }
-    const int i = row / a.P, piece = row - i * a.P;
-    const int tok = sh ? g.pos0 + i : perm[g.pos0 + i] / a.k;
-    const float sc = tscale[tok];
-    if (lane == 0 && part == 0) a.rscale[g.xrow0 + row] = 1.0f / sc;
+    const int nj = min(32, nr - jb);
+    for (int jj = 0; jj < nj; jj++) {
+      const int row = r0 + (jb + jj) * rstep;
+      const int tok = __shfl_sync(0xffffffffu, ltok, jj);
+      const float sc = __shfl_sync(0xffffffffu, lsc, jj);
+      if (row >= rows) {
+        for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr)
+          *(uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4)) =
+              make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      const int piece = row - (row / a.P) * a.P;
 #pragma unroll 8
-    for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr) {
-      const size_t col = (size_t)kc * kKChunk + c * 8;
-      float f[8];
-      if (is_bf16) {
-        const uint4 u = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
-        const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+      for (int kc = 4 * part + (lane >> 3); kc < KC; kc += 4 * wpr) {
+        const size_t col = (size_t)kc * kKChunk + c * 8;
+        float f[8];
+        if (is_bf16) {
+          const uint4 u = *(const uint4 *)((const uint16_t *)x + (size_t)tok * a.H + col);
+          const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int m = 0; m < 4; m++) {
+            f[2 * m] = __uint_as_float(q[m] << 16);
+            f[2 * m + 1] = __uint_as_float(q[m] & 0xFFFF0000u);
+          }
+        } else {
+          const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
+          const float4 f0 = src[0], f1 = src[1];
+          f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
+          f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
+        }
+        uint32_t o[4];
 #pragma unroll
         for (int m = 0; m < 4; m++) {
-          f[2 * m] = __uint_as_float(q[m] << 16);
-          f[2 * m + 1] = __uint_as_float(q[m] & 0xFFFF0000u);
+          const float v0 = f[2 * m] * sc, v1 = f[2 * m + 1] * sc;  // exact: sc is a power of two
+          __half2 hv = __floats2half2_rn(v0, v1);
+          if (piece) hv = __floats2half2_rn(v0 - __low2float(hv), v1 - __high2float(hv));
+          o[m] = *(uint32_t *)&hv;
         }
-      } else {
-        const float4 *src = (const float4 *)((const float *)x + (size_t)tok * a.H + col);
-        const float4 f0 = src[0], f1 = src[1];
-        f[0] = f0.x; f[1] = f0.y; f[2] = f0.z; f[3] = f0.w;
-        f[4] = f1.x; f[5] = f1.y; f[6] = f1.z; f[7] = f1.w;
+        *(uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
       }
-      uint32_t o[4];
-#pragma unroll
-      for (int m = 0; m < 4; m++) {
-        const float v0 = f[2 * m] * sc, v1 = f[2 * m + 1] * sc;  // exact: sc is a power of two
-        __half2 hv = __floats2half2_rn(v0, v1);
-        if (piece) hv = __floats2half2_rn(v0 - __low2float(hv), v1 - __high2float(hv));
-        o[m] = *(uint32_t *)&hv;
-      }
-      *(uint4 *)(base + ((size_t)kc * rows8 + row) * 128 + ((c ^ (row & 7)) << 4)) =
-          make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }

@@ -113,7 +113,7 @@ static int check(const moe_layer_config *c) {
 
 static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
-// largest T one call supports: the permutation's per-chunk tables live in shared memory
+// largest T one call supports (slot positions and token indices stay well inside int)
 static bool tokens_supported(const moe_layer_config &c, int T) {
   if (T > 65535) return false;
   return (long)permute_smem(T, c.n_experts) <= (long)dev_info().smem_optin;

@@ -247,6 +247,23 @@ def test_layer_decode_rows_without_gemv_router():
     check_layer(small("softmax", hidden=12416, inter=256), 16, seed=9)
 
 
+@pytest.mark.parametrize("top_p", [0.0, 0.6])
+def test_permutation_past_one_chunk_per_cta(top_p):
+    """Past two 32-token chunks per SM, each permutation CTA scatters a run of chunks: the
+    offsets and perm stay bit-identical to the oracle's stable order (with top-p, the
+    dropped slots form perm's -1 tail)."""
+    s = gen.spec("tiny").replace(top_p=top_p)
+    T = 12000
+    L = get_layer(s, 5)
+    x, xd, ids_o, w_o, *_ = inputs(s, L, 0, T)
+    out, ids, w = L.forward(xd)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    off_o, perm_o = oracle.permutation(ids_o, s.n_experts)
+    off_g, perm_g = L.permutation(T)
+    print(f"tiny T={T} top_p={top_p}: {int((ids_o < 0).sum())} slots dropped")
+    assert np.array_equal(off_g, off_o) and np.array_equal(perm_g, perm_o)
+
+
 def test_layer_deterministic_and_T0_noop():
     s = small("grouped")
     L = get_layer(s, 1)
