@@ -356,12 +356,13 @@ def run_ours(a, rank, ws_n, local):
 
     # e2e: the public C-ABI call on device buffers filled from pinned host memory, the
     # results read back to pinned host memory, every step's copies inside the timed region.
-    # The copies run on their own stream and overlap the neighbouring steps' forwards (step
-    # i+1's input goes in and step i-1's output comes out while step i computes; device
-    # buffers are double-buffered per T, with events ordering every reuse).  Every forward
-    # reads more than L2 holds (>= 170 MB of unique experts), so no flush is needed.
+    # Inputs go in on one copy stream and results come out on another (the two directions
+    # run on separate copy engines), so step i+1's input goes in and step i-1's results come
+    # out while step i computes; device buffers are double-buffered per T, with events
+    # ordering every reuse.  Every forward reads more than L2 holds (>= 170 MB of unique
+    # experts), so no flush is needed.
     comp = torch.cuda.current_stream()
-    cps = torch.cuda.Stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
     xb = {T: [torch.empty_like(xs[T][0]) for _ in range(2)] for T in TS}
     ob = {T: [torch.empty_like(out[T]) for _ in range(2)] for T in TS}
     ib = {T: [torch.empty_like(ids[T]) for _ in range(2)] for T in TS}
@@ -377,32 +378,41 @@ def run_ours(a, rank, ws_n, local):
         e_end = torch.cuda.Event(enable_timing=True)
         barrier(ws_n)
         torch.cuda.synchronize()
-        e_start.record(cps)
+        e_start.record(h2d_s)
+        d2h_s.wait_event(e_start)
+        comp.wait_event(e_start)
         last = {}  # per (T, buffer slot): index in seq of its previous use
+
+        def copy_in(n):
+            i, T = seq[n]
+            prev = last.get((T, i % 2))
+            with torch.cuda.stream(h2d_s):
+                if prev is not None:
+                    h2d_s.wait_event(ev_fwd[prev])  # the forward that read this input buffer
+                xb[T][i % 2].copy_(xh[T][i % N_BATCHES], non_blocking=True)
+                ev_in[n].record(h2d_s)
+
+        copy_in(0)
         for n, (i, T) in enumerate(seq):
             slot = i % 2
             prev = last.get((T, slot))
-            with torch.cuda.stream(cps):
-                if prev is not None:
-                    cps.wait_event(ev_fwd[prev])  # the forward that read this input buffer
-                xb[T][slot].copy_(xh[T][i % N_BATCHES], non_blocking=True)
-                ev_in[n].record(cps)
             comp.wait_event(ev_in[n])
             if prev is not None:
                 comp.wait_event(ev_out[prev])  # the copies that read these result buffers
             moe.moe_layer_forward(cfg, packed, xb[T][slot], ob[T][slot], ib[T][slot],
                                   wb[T][slot], ws)
             ev_fwd[n].record(comp)
-            with torch.cuda.stream(cps):
-                cps.wait_event(ev_fwd[n])
+            last[(T, slot)] = n
+            if n + 1 < len(seq):
+                copy_in(n + 1)  # the next input, while this forward runs
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_fwd[n])
                 out_h[T].copy_(ob[T][slot], non_blocking=True)
                 ids_h[T].copy_(ib[T][slot], non_blocking=True)
                 w_h[T].copy_(wb[T][slot], non_blocking=True)
-                ev_out[n].record(cps)
-            last[(T, slot)] = n
-        with torch.cuda.stream(cps):
-            cps.wait_event(ev_fwd[len(seq) - 1])
-            e_end.record(cps)
+                ev_out[n].record(d2h_s)
+        d2h_s.wait_event(ev_fwd[len(seq) - 1])
+        e_end.record(d2h_s)  # after the last results are copied out
         torch.cuda.synchronize()
         return e_start.elapsed_time(e_end)
 
