@@ -50,8 +50,8 @@ struct Item {
 
 template <bool DOWN>
 __device__ __forceinline__ bool tc_item(const TcArgs &a, int item, Item &it) {
-  // through L2: the down kernel's producer reads the work list before pdl_wait (it was
-  // written two launches back)
+  // through L2 (every role reads the work list, written by earlier launches, after the
+  // kernel's griddepcontrol.wait)
   const int n_groups = __ldcg(&a.ctrl->n_groups);
   const int mt_s = DOWN ? a.H / 128 : a.LS.inter / 64;
   const int mt_r = DOWN ? a.H / 128 : a.LR.inter / 64;

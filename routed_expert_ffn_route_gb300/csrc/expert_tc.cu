@@ -7,8 +7,8 @@
 //
 // Tensor-core formulation (one CTA per SM, persistent over (group, m-tile) work items):
 //   D[128 weight rows][N] (fp32, TMEM) += A[128][K] * B[N][K]^T
-//   A = codes of 128 weight rows, dequantised to exact small integers in bf16 (gate/up,
-//       against bf16 x) or fp16 (down, against fp16 h) and written to TMEM, so the weight
+//   A = codes of 128 weight rows, dequantised to exact small integers in fp16 (against
+//       fp16 activation tiles: scaled x, or h) and written to TMEM, so the weight
 //       operand costs no shared-memory read bandwidth (tcgen05.mma with A in TMEM);
 //   B = the group's activation rows (<= 128 tokens x pieces, padded to a multiple of 8), a
 //       128-byte-swizzled K-major tile produced in that exact layout in global memory; the
