@@ -159,8 +159,11 @@ __device__ __forceinline__ void dq_word_i8(uint32_t w, uint32_t *o) {
 }
 
 // Small-group expert GEMMs (every group's B rows <= kMmaMaxRows): register-MMA kernel.
+// Down launches split each item's contraction into ks parts (ks must divide every item's
+// count of code runs), part sp > 0 writing y plane sp at ysplit + (sp - 1) * yplane floats.
 int launch_experts_mma(int bits, bool down, TcArgs a, int rows_max, int kc_gcd, int bound,
-                       int sms, cudaStream_t st);
+                       int sms, cudaStream_t st, int ks = 1, float *ysplit = nullptr,
+                       long yplane = 0);
 size_t mma_smem_bytes(int bits);
 
 }  // namespace moe

@@ -23,6 +23,9 @@
 //  - The epilogue is per warp: per-row scale, SwiGLU across the interleaved gate/up rows
 //    (adjacent rows sit 4 lanes apart in the accumulator fragment), and the same outputs
 //    as the tensor-memory kernel (fp16 h tiles for the down projection, fp32 y rows).
+//  - A down launch with few work items (see down_splits) splits each item's contraction
+//    into `ks` contiguous parts: work item i is part i % ks of item i / ks, and part sp
+//    writes y plane sp (plane 0 is y, planes 1.. follow at ysplit, yplane floats apart).
 //
 // K order inside a 64-element chunk.  A dot product does not depend on the order of its
 // terms, so the MMA's k slots may take the chunk's elements in any order, as long as A and
@@ -94,7 +97,9 @@ __device__ __forceinline__ void dequant_quarter(const uint8_t *q, uint32_t (&o)[
 }
 
 template <int BITS, bool DOWN, int NT, int RA>
-__global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, int item_bound) {
+__global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, int item_bound,
+                                                                     int ks, float *ysplit,
+                                                                     long yplane) {
   using PL = MmaPlan<BITS>;
   constexpr int S = PL::stages, AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
   constexpr int RS = RA * 128 + 16;  // gate/up: bytes of one activation row in a stage
@@ -143,8 +148,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
       };
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
-        if (!tc_item<DOWN>(a, item, it)) break;
-        for (int kc = 0; kc < it.KC; kc += RA, run++) {
+        const int base = item / ks, sp = item - base * ks;
+        if (!tc_item<DOWN>(a, base, it)) break;
+        const int kpart = it.KC / ks;
+        for (int kc = sp * kpart; kc < (sp + 1) * kpart; kc += RA, run++) {
           if (!waited && run == S) release(S);
           const int s = run % S;
           const uint32_t ph = (run / S) & 1;
@@ -234,7 +241,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
     bool ok = true;
     Item it;
     for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
-      if (!tc_item<DOWN>(a, item, it)) break;
+      const int base = DOWN ? item / ks : item, sp = DOWN ? item - base * ks : 0;
+      if (!tc_item<DOWN>(a, base, it)) break;
+      const int kpart = it.KC / (DOWN ? ks : 1);
       const int nt = it.rows8 >> 3;  // 8-row activation tiles of this group (<= NT)
       const int bstride = it.rows8 * 128;
       float acc[NT][2][4];
@@ -242,7 +251,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
       for (int n = 0; n < NT; n++)
 #pragma unroll
         for (int i = 0; i < 4; i++) acc[n][0][i] = acc[n][1][i] = 0.f;
-      for (int kc0 = 0; kc0 < it.KC; kc0 += RA, run++) {
+      for (int kc0 = sp * kpart; kc0 < (sp + 1) * kpart; kc0 += RA, run++) {
         const int s = run % S;
         const uint32_t ph = (run / S) & 1;
         ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->full[s], ph, abort, lim));
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
         const float *sd = (const float *)(it.ebase + L.sd_off) + it.mt * 128;
         const float s0 = sd[r0], s1 = sd[r1];
         const long yrow0 = it.sh ? (long)a.T * a.k + it.g.pos0 : (long)it.g.pos0;
-        float *ybase = a.y + yrow0 * a.H + it.mt * 128;
+        float *ybase = (sp ? ysplit + (sp - 1) * yplane : a.y) + yrow0 * a.H + it.mt * 128;
 #pragma unroll
         for (int n = 0; n < NT; n++) {
           if (n >= nt) break;
@@ -347,40 +356,49 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_expert_kernel(TcArgs a, in
 }
 
 template <int BITS, bool DOWN, int NT, int RA>
-static int launch_mma(const TcArgs &a, int bound, int sms, cudaStream_t st) {
+static int launch_mma(const TcArgs &a, int bound, int sms, cudaStream_t st, int ks,
+                      float *ysplit, long yplane) {
   auto k = mma_expert_kernel<BITS, DOWN, NT, RA>;
   constexpr size_t smem = MmaPlan<BITS>::smem;
   set_dyn_smem((const void *)k, (int)smem);
   const int grid = 2 * sms < bound ? 2 * sms : bound;  // two CTAs per SM
-  if (launch_pdl(k, dim3(grid), dim3(kMmaThreads), smem, st, a, bound) != cudaSuccess)
+  if (launch_pdl(k, dim3(grid), dim3(kMmaThreads), smem, st, a, bound, ks, ysplit, yplane) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <int BITS, bool DOWN, int NT>
-static int launch_mma_ra(const TcArgs &a, int kc_gcd, int bound, int sms, cudaStream_t st) {
-  if (kc_gcd % 4 == 0) return launch_mma<BITS, DOWN, NT, 4>(a, bound, sms, st);
-  if (kc_gcd % 2 == 0) return launch_mma<BITS, DOWN, NT, 2>(a, bound, sms, st);
-  return launch_mma<BITS, DOWN, NT, 1>(a, bound, sms, st);
+static int launch_mma_ra(const TcArgs &a, int kc_gcd, int bound, int sms, cudaStream_t st,
+                         int ks, float *ysplit, long yplane) {
+  if (kc_gcd % 4 == 0) return launch_mma<BITS, DOWN, NT, 4>(a, bound, sms, st, ks, ysplit, yplane);
+  if (kc_gcd % 2 == 0) return launch_mma<BITS, DOWN, NT, 2>(a, bound, sms, st, ks, ysplit, yplane);
+  return launch_mma<BITS, DOWN, NT, 1>(a, bound, sms, st, ks, ysplit, yplane);
 }
 
 template <int BITS>
 static int launch_mma_bits(bool down, const TcArgs &a, bool two, int kc_gcd, int bound, int sms,
-                           cudaStream_t st) {
-  if (down) return two ? launch_mma_ra<BITS, true, 2>(a, kc_gcd, bound, sms, st)
-                       : launch_mma_ra<BITS, true, 1>(a, kc_gcd, bound, sms, st);
-  return two ? launch_mma_ra<BITS, false, 2>(a, kc_gcd, bound, sms, st)
-             : launch_mma_ra<BITS, false, 1>(a, kc_gcd, bound, sms, st);
+                           cudaStream_t st, int ks, float *ysplit, long yplane) {
+  if (down)
+    return two ? launch_mma_ra<BITS, true, 2>(a, kc_gcd, bound, sms, st, ks, ysplit, yplane)
+               : launch_mma_ra<BITS, true, 1>(a, kc_gcd, bound, sms, st, ks, ysplit, yplane);
+  return two ? launch_mma_ra<BITS, false, 2>(a, kc_gcd, bound, sms, st, 1, nullptr, 0)
+             : launch_mma_ra<BITS, false, 1>(a, kc_gcd, bound, sms, st, 1, nullptr, 0);
 }
 
 int launch_experts_mma(int bits, bool down, TcArgs a, int rows_max, int kc_gcd, int bound,
-                       int sms, cudaStream_t st) {
+                       int sms, cudaStream_t st, int ks, float *ysplit, long yplane) {
   if (rows_max > kMmaMaxRows) return MOE_ERR_UNSUPPORTED;
+  // every item's code runs split evenly: ks divides kc_gcd / (chunks per run)
+  const int ra = kc_gcd % 4 == 0 ? 4 : (kc_gcd % 2 == 0 ? 2 : 1);
+  if (!down) ks = 1;
+  if (ks < 1 || (kc_gcd / ra) % ks || (ks > 1 && !ysplit)) return MOE_ERR_INVALID_ARG;
+  const int items = (long)bound * ks > 0x7fffffff ? 0x7fffffff : bound * ks;
   const bool two = rows_max > 8;
   switch (bits) {
-    case 4: return launch_mma_bits<4>(down, a, two, kc_gcd, bound, sms, st);
-    case 2: return launch_mma_bits<2>(down, a, two, kc_gcd, bound, sms, st);
-    case 8: return launch_mma_bits<8>(down, a, two, kc_gcd, bound, sms, st);
+    case 4: return launch_mma_bits<4>(down, a, two, kc_gcd, items, sms, st, ks, ysplit, yplane);
+    case 2: return launch_mma_bits<2>(down, a, two, kc_gcd, items, sms, st, ks, ysplit, yplane);
+    case 8: return launch_mma_bits<8>(down, a, two, kc_gcd, items, sms, st, ks, ysplit, yplane);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

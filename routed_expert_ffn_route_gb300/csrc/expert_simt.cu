@@ -266,7 +266,8 @@ __global__ void __launch_bounds__(256) down_kernel(ExpertArgs a, int item_bound)
 // issued before the wait, it depends on nothing this launch reads.
 __global__ void combine_kernel(int T, int H, int k, int n_shared, const float *w,
                                const int32_t *slot_pos, const float *y, float *out,
-                               const uint8_t *pf, uint64_t pf_bytes) {
+                               const uint8_t *pf, uint64_t pf_bytes, int ks,
+                               const float *ysplit, long yplane) {
   if (pf && threadIdx.x < 32) {
     constexpr uint64_t kSlice = 32 * 1024;
     for (uint64_t off = ((uint64_t)blockIdx.x * 32 + threadIdx.x) * kSlice; off < pf_bytes;
@@ -282,13 +283,25 @@ __global__ void combine_kernel(int T, int H, int k, int n_shared, const float *w
   if (i >= (long)T * per_t) return;
   int t = (int)(i / per_t);
   int c4 = (int)(i % per_t);
+  // a y row: plane 0, plus planes 1.. in order when the down launch split its contraction
+  auto yrow = [&](long r) {
+    float4 v = ((const float4 *)(y + r * H))[c4];
+    for (int p = 1; p < ks; p++) {
+      const float4 u = ((const float4 *)(ysplit + (p - 1) * yplane + r * H))[c4];
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+    return v;
+  };
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (n_shared) acc = ((const float4 *)(y + ((long)T * k + t) * H))[c4];
+  if (n_shared) acc = yrow((long)T * k + t);
   for (int j = 0; j < k; j++) {
     const int sp = slot_pos[t * k + j];
     if (sp < 0) continue;  // dropped by top-p, or an expert outside the call's share
     float wj = w[t * k + j];
-    float4 v = ((const float4 *)(y + (long)sp * H))[c4];
+    float4 v = yrow(sp);
     acc.x = fmaf(wj, v.x, acc.x);
     acc.y = fmaf(wj, v.y, acc.y);
     acc.z = fmaf(wj, v.z, acc.z);
@@ -392,7 +405,8 @@ int launch_combine(const moe_layer_config &c, int T, const float *w, float *out,
   long n = (long)T * (c.hidden / 4);
   if (launch_pdl(combine_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, T, c.hidden,
                  c.top_k, c.n_shared && W.shared ? 1 : 0, w, (const int32_t *)(ws + W.slot_pos),
-                 (const float *)(ws + W.y), out, pf, pf_bytes) != cudaSuccess)
+                 (const float *)(ws + W.y), out, pf, pf_bytes, W.ks,
+                 (const float *)(ws + W.ysplit), (long)W.rows * c.hidden) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -630,7 +630,7 @@ static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
 template <int BITS>
 static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16,
                   const int32_t *perm, const float *tscale, cudaStream_t st, void *act,
-                  void *mid, bool front_rows) {
+                  void *mid, bool front_rows, float *ysplit) {
   DevInfo d = dev_info();
   if ((long)tc_smem<128, BITS>() > d.smem_optin || (long)tc_smem<32, BITS>() > d.smem_optin ||
       (long)mma_smem_bytes(BITS) > d.smem_optin)
@@ -672,8 +672,11 @@ static int run_tc(const TcArgs &a, const WsLayout &W, const void *x, int is_bf16
   TcArgs ad = a;
   ad.trace = nullptr;  // traces (development builds) cover the gate/up kernel
   const int kc_dn = gcd_i(a.LR.inter / kKChunk, a.LS.inter / kKChunk);
+  // only the register-MMA down launch splits its contraction (the combine adds W.ks planes)
+  if (W.ks > 1 && grows > kMmaMaxRows) return MOE_ERR_UNSUPPORTED;
   return grows <= kMmaMaxRows
-             ? launch_experts_mma(BITS, true, ad, grows, kc_dn, bound_dn, d.sms, st)
+             ? launch_experts_mma(BITS, true, ad, grows, kc_dn, bound_dn, d.sms, st, W.ks,
+                                  W.ks > 1 ? ysplit : nullptr, (long)W.rows * a.H)
              : launch_tc_n<BITS, true>(ad, grows, kc_dn, bound_dn, d.sms, st);
 }
 
@@ -711,10 +714,11 @@ int launch_experts_tc(const moe_layer_config &c, const uint8_t *packed, const vo
   const int32_t *perm = (const int32_t *)(ws + W.perm);
   a.perm = perm;
   const int is_bf16 = dt == MOE_DT_BF16;
+  float *ysplit = (float *)(ws + W.ysplit);  // y planes 1.. of a split down launch
   switch (c.weight_bits) {
-    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows);
-    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows);
-    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows);
+    case 4: return run_tc<4>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows, ysplit);
+    case 2: return run_tc<2>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows, ysplit);
+    case 8: return run_tc<8>(a, W, x, is_bf16, perm, tscale, st, act, mid, front_rows, ysplit);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

@@ -118,8 +118,9 @@ static inline bool use_tc(const moe_layer_config &c) { return !c.act_q8_0; }
 
 struct WsLayout {
   uint64_t ctrl, partials, offsets, perm, slot_pos, groups, xq, xd, tscale, rscale, xg, hg, h,
-      y, total;
+      y, ysplit, total;
   int max_groups, group_n, rows, pieces;
+  int ks;  // contraction parts of the decode down launch (y planes: y, then ks - 1 at ysplit)
   bool tc;
   // The experts this call computes: routed experts [e0, e1) and, when `shared` is set, the
   // shared expert (an expert-parallel share of the layer; the whole layer by default).
@@ -130,6 +131,31 @@ struct WsLayout {
 
 int choose_group_n(const moe_layer_config &c, int T);
 size_t permute_smem(int T, int E);
+
+static inline int gcd_int(int x, int y) { return y ? gcd_int(y, x % y) : x; }
+
+// The decode down launch (the register-MMA kernel: T <= kMmaMaxRows) has one work item per
+// (expert, 128-row m-tile of H).  When the batch's experts give fewer items than about
+// kDownSplitItems (a few experts with a long contraction, e.g. a Mixtral-shaped layer at
+// T = 1: 2 experts x 32 m-tiles against ~300 CTAs), each item's contraction is split into
+// ks contiguous parts (a power of two dividing every item's count of code runs), each part
+// writing its own y plane, which the combine adds in plane order.  The item count is
+// estimated from the config (the experts a batch of T tokens can reach), so ks only falls
+// as T grows; the DeepSeek-V3-shaped layer (>= 9 experts x 48 m-tiles) never splits.
+constexpr int kDownSplitItems = 256;
+constexpr int kDownSplitMax = 8;
+static inline int down_splits(const moe_layer_config &c, int T) {
+  if (c.act_q8_0 || T < 1 || T > kMmaMaxRows) return 1;
+  const int Is = c.inter_shared ? c.inter_shared : c.inter;
+  const int kc = gcd_int(c.inter / 64, Is / 64);  // as the launch computes it
+  const int ra = kc % 4 == 0 ? 4 : (kc % 2 == 0 ? 2 : 1);  // chunks per code run
+  const int runs = kc / ra;
+  const long items = (long)((c.n_experts < T * c.top_k ? c.n_experts : T * c.top_k) +
+                            (c.n_shared ? 1 : 0)) * (c.hidden / 128);
+  int s = 1;
+  while (s < kDownSplitMax && items * 2 * s <= kDownSplitItems && runs % (2 * s) == 0) s *= 2;
+  return s;
+}
 
 // `pieces`: fp16 rows per token in the tensor-core B operand (1 for bf16 x, 2 for fp32 x
 // split as hi + lo).  Region offsets and the total do not depend on it.
@@ -168,6 +194,16 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   W.hg = o; o = align_up(o + hg_rows * Imax * 2, 256);
   W.h = o; o = align_up(o + (W.tc ? 0 : (uint64_t)W.rows * Imax * 4), 256);
   W.y = o; o = align_up(o + (uint64_t)W.rows * c.hidden * 4, 256);
+  // planes 1.. of a split decode down launch: sized for the most parts any T' <= T takes
+  // (T' = 1) times the rows of min(T, kMmaMaxRows) tokens, so a workspace sized for T
+  // holds every smaller call's planes
+  W.ks = down_splits(c, T);
+  {
+    const int t16 = T < kMmaMaxRows ? T : kMmaMaxRows;
+    const uint64_t rows16 = (uint64_t)t16 * k + (c.n_shared ? t16 : 0);
+    W.ysplit = o;
+    o = align_up(o + (uint64_t)(down_splits(c, 1) - 1) * rows16 * c.hidden * 4, 256);
+  }
   W.total = o;
   return W;
 }

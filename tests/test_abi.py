@@ -138,6 +138,23 @@ def test_workspace_grows_with_tokens(L):
     assert b >= 2048 * 9 * 6144 * 4  # the fp32 expert outputs of every (token, slot)
 
 
+# a Mixtral-shaped small layer: few experts, a long down contraction (the decode down
+# launch splits its work items' contractions and needs room for the extra y planes)
+MIX_SPLIT = gen.LayerSpec("mix_split", hidden=1024, inter=2048, n_experts=8, top_k=2,
+                          router="softmax")
+
+
+@pytest.mark.parametrize("spec", [gen.spec("dsv3"), gen.spec("tiny"), MIX_SPLIT,
+                                  MIX_SPLIT.replace(n_shared=1, inter_shared=1024)],
+                         ids=["dsv3", "tiny", "mix_split", "mix_split_shared"])
+def test_workspace_never_shrinks_as_tokens_grow(spec, L):
+    """A workspace sized for T tokens serves every call of T' <= T tokens, so the size is
+    monotone in T (the split down launch's extra y planes are largest at small T)."""
+    cfg = config_for(spec)
+    sizes = [moe.moe_workspace_bytes(cfg, T) for T in list(range(1, 41)) + [64, 512, 4096]]
+    assert all(0 < a <= b for a, b in zip(sizes, sizes[1:])), sizes
+
+
 def test_forward_launch_counts(L):
     """Decode-sized batches run as one front launch (router, selection, permutation,
     token rows) plus gate/up, down and combine; other batches take the separate launches."""

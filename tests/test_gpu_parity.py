@@ -247,6 +247,22 @@ def test_layer_decode_rows_without_gemv_router():
     check_layer(small("softmax", hidden=12416, inter=256), 16, seed=9)
 
 
+# A Mixtral-shaped small layer: few experts with a long down contraction, so the decode
+# down launch has few work items and splits each item's contraction (8 parts at T = 1 and
+# 2, 4 at T = 5 and 16; 4 with the shared expert), the combine adding the parts' y planes.
+MIX_SPLIT = gen.LayerSpec("mix_split", hidden=1024, inter=2048, n_experts=8, top_k=2,
+                          router="softmax")
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 16])
+@pytest.mark.parametrize("shared", [0, 1])
+def test_layer_split_down_contraction(T, shared):
+    s = MIX_SPLIT.replace(n_shared=shared, inter_shared=1024 if shared else 0)
+    out, ids, w, xd, L = check_layer(s, T)  # every output element against the oracle
+    again, _, _ = L.forward(xd)
+    assert torch.equal(out, again)  # the planes are added in a fixed order
+
+
 @pytest.mark.parametrize("top_p", [0.0, 0.6])
 def test_permutation_past_one_chunk_per_cta(top_p):
     """Past two 32-token chunks per SM, each permutation CTA scatters a run of chunks: the
