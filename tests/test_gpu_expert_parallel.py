@@ -122,6 +122,25 @@ def test_full_size_two_shares(T):
         share_close(p.cpu().numpy()[tok], ref, layer, f"dsv3 T={T} share [{b},{e}) shared={sh}")
 
 
+def test_split_down_shares_sum_to_layer():
+    """At T = 1 the Mixtral-shaped layer's down launch splits each work item's contraction;
+    two expert shares, each with its own split launch and planes, still add up to the
+    layer."""
+    s = gen.LayerSpec("ep_mix_split", hidden=1024, inter=2048, n_experts=8, top_k=2,
+                      router="softmax")
+    L = get_layer(s, 3)
+    x, xd, ids_o, w_o, *_ = inputs(s, L, 4, 1)
+    full, _, _ = L.forward(xd)
+    parts = [share_forward(L, xd, b, e, 0)[0] for b, e, _ in shares(s.n_experts, 2)]
+    mx, fr = err_stats((parts[0] + parts[1]).cpu().numpy(), full.cpu().numpy())
+    print(f"mix_split T=1: two shares summed vs the layer: {mx:.2e} / {fr:.2e}")
+    assert mx <= 1e-5 and fr <= 1e-6
+    layer = oracle_out(s, L, x, ids_o, w_o)
+    for (b, e, _), p in zip(shares(s.n_experts, 2), parts):
+        share_close(p.cpu().numpy(), oracle_share(L, x, ids_o, w_o, b, e, 0, np.arange(1)),
+                    layer, f"mix_split T=1 share [{b},{e})")
+
+
 def _rank(rank, world, port, T, q):
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))

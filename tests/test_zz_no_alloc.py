@@ -58,8 +58,14 @@ SMALL = gen.LayerSpec("noalloc_small", hidden=512, inter=384, n_experts=16, top_
                       topk_group=2, rsf=2.5, bias_std=0.1)
 
 
+# Mixtral-shaped: at T = 1 the down launch splits its contraction into 8 parts, whose
+# extra y planes live in the static array too
+MIX_SPLIT = gen.LayerSpec("noalloc_mix_split", hidden=1024, inter=2048, n_experts=8, top_k=2,
+                          router="softmax")
+
+
 @pytest.mark.parametrize("spec,T", [(SMALL, 37), (gen.spec("dsv3"), 16),
-                                    (gen.spec("dsv3"), "largest")])
+                                    (gen.spec("dsv3"), "largest"), (MIX_SPLIT, 1)])
 def test_static_scratch_forward_matches_workspace_forward(spec, T):
     L = GpuLayer(spec, seed=21)
     if T == "largest":
