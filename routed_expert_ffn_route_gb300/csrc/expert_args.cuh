@@ -43,23 +43,33 @@ struct ATile {
 
 struct Item {
   Group g;
-  int mt, K, KC, rowsB, rows8, Npad;
+  int mt, nmt, K, KC, rowsB, rows8, Npad;  // first m-tile, m-tiles of the item (1 or MT)
   bool sh;
   const uint8_t *ebase;
 };
 
-template <bool DOWN>
+// Work item `item` of a launch whose items are MT consecutive m-tiles of one group (the
+// last item of a group takes fewer when MT does not divide the group's m-tiles).
+template <bool DOWN, int MT = 1>
 __device__ __forceinline__ bool tc_item(const TcArgs &a, int item, Item &it) {
   // through L2 (every role reads the work list, written by earlier launches, after the
   // kernel's griddepcontrol.wait)
   const int n_groups = __ldcg(&a.ctrl->n_groups);
-  const int mt_s = DOWN ? a.H / 128 : a.LS.inter / 64;
-  const int mt_r = DOWN ? a.H / 128 : a.LR.inter / 64;
+  const int nm_s = DOWN ? a.H / 128 : a.LS.inter / 64;  // m-tiles of a shared-expert group
+  const int nm_r = DOWN ? a.H / 128 : a.LR.inter / 64;
+  const int mt_s = (nm_s + MT - 1) / MT, mt_r = (nm_r + MT - 1) / MT;  // items per group
   const int shi = a.ns * mt_s;
   if (item >= shi + (n_groups - a.ns) * mt_r) return false;
-  int gi;
-  if (item < shi) { gi = item / mt_s; it.mt = item % mt_s; it.sh = true; }
-  else { int i2 = item - shi; gi = a.ns + i2 / mt_r; it.mt = i2 % mt_r; it.sh = false; }
+  int gi, nm;
+  if (item < shi) { gi = item / mt_s; it.mt = (item % mt_s) * MT; it.sh = true; nm = nm_s; }
+  else {
+    int i2 = item - shi;
+    gi = a.ns + i2 / mt_r;
+    it.mt = (i2 % mt_r) * MT;
+    it.sh = false;
+    nm = nm_r;
+  }
+  it.nmt = nm - it.mt < MT ? nm - it.mt : MT;
   {
     const int4 *gp = (const int4 *)(a.groups + gi);
     const int4 g0 = __ldcg(gp), g1 = __ldcg(gp + 1);
@@ -75,12 +85,14 @@ __device__ __forceinline__ bool tc_item(const TcArgs &a, int item, Item &it) {
   return true;
 }
 
-// codes of chunk kc of the item's matrix (consecutive chunks are contiguous)
+// codes of chunk kc of m-tile it.mt + m of the item's matrix (consecutive chunks are
+// contiguous)
 template <int BITS, bool DOWN>
-__device__ __forceinline__ const uint8_t *a_src(const TcArgs &a, const Item &it, int kc) {
+__device__ __forceinline__ const uint8_t *a_src(const TcArgs &a, const Item &it, int kc,
+                                                int m = 0) {
   const ExpertLayout &L = it.sh ? a.LS : a.LR;
   return it.ebase + (DOWN ? L.down_off : L.gu_off) +
-         ((size_t)it.mt * it.KC + kc) * ATile<BITS>::bytes;
+         ((size_t)(it.mt + m) * it.KC + kc) * ATile<BITS>::bytes;
 }
 
 // the item's activation tile of chunk kc (consecutive chunks are contiguous)

@@ -5,30 +5,35 @@
 // 使用时反量化; "colibrì 深度拆解", §5.1 per-row scaled int4):
 //   g = s_g * (Q_g x),  u = s_u * (Q_u x),  h = silu(g) * u,  y = s_d * (Q_d h)
 //
-// Tensor-core formulation (one CTA per SM, persistent over (group, m-tile) work items):
-//   D[128 weight rows][N] (fp32, TMEM) += A[128][K] * B[N][K]^T
+// Tensor-core formulation (one CTA per SM, persistent over work items of one group and
+// one or two m-tiles of 128 weight rows):
+//   D[128 weight rows][N] (fp32, TMEM) += A[128][K] * B[N][K]^T, per m-tile
 //   A = codes of 128 weight rows, dequantised to exact small integers in fp16 (against
 //       fp16 activation tiles: scaled x, or h) and written to TMEM, so the weight
 //       operand costs no shared-memory read bandwidth (tcgen05.mma with A in TMEM);
 //   B = the group's activation rows (<= 128 tokens x pieces, padded to a multiple of 8), a
 //       128-byte-swizzled K-major tile produced in that exact layout in global memory; the
 //       MMA's N is the row count rounded up to 16, and the extra rows it reads only feed
-//       accumulator columns the epilogue never reads;
+//       accumulator columns the epilogue never reads; one tile serves both m-tiles of a
+//       two-m-tile item;
 //   the fp32 per-row scale factors out of each dot and is applied in the epilogue.
 //
 // The K dimension streams in 64-element chunks.  Operands move in runs of several chunks
-// per bulk copy (codes: RA chunks = RA x 4 KB at int4; activation tiles: RB chunks), so
-// the hand-off latency of a copy (its stage must first be released by the consumers) is
-// paid once per run.  A chunk's dequantised codes live in one of up to 15 TMEM stages
-// (32 columns each) next to the accumulators.
+// per bulk copy (codes: RA chunks of each of the item's m-tiles, RA x 4 KB at int4;
+// activation tiles: RB chunks), so the hand-off latency of a copy (its stage must first be
+// released by the consumers) is paid once per run.  A unit of two chunks (of every m-tile
+// of the item) of dequantised codes lives in one of the TMEM stages next to the
+// accumulators; the unit's stage hand-off between dequantisers and MMA issuer costs about
+// the same whether it carries 8 MMAs or 16, so narrow launches (groups of <= 64 rows,
+// where TMEM has room) take two m-tiles per item.
 //
 // Warp roles: 20 code producer and 21 activation-tile producer (bulk copies, one thread
 // each), 0 MMA issuer (the warp runs the loop, one elected thread issues; items alternate
-// between two TMEM accumulators), 8-19 dequantisers in three sets that take turns by chunk
-// (one weight row per thread, smem -> registers -> TMEM), 4-7 epilogue (TMEM -> registers,
-// scale, SwiGLU, stores; overlaps the next item's MMAs).  Every wait is bounded: a wait that gives up
-// records MOE_ERR_TIMEOUT, all roles stop, in-flight copies and MMAs are drained and TMEM
-// is freed before exit.
+// between two TMEM accumulator buffers), 8-19 dequantisers in three sets that take turns
+// by unit (one weight row of each m-tile per thread, smem -> registers -> TMEM; no more
+// sets than stages), 4-7 epilogue (TMEM -> registers, scale, SwiGLU, stores; overlaps the
+// next item's MMAs).  Every wait is bounded: a wait that gives up records MOE_ERR_TIMEOUT,
+// all roles stop, in-flight copies and MMAs are drained and TMEM is freed before exit.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -91,12 +96,18 @@ constexpr int kMaxRuns = 24;
 // the next.  TMEM (512 columns) holds the two accumulators and up to 15 chunk stages of
 // dequantised codes (32 columns each).  Shared memory holds the code-run ring and the
 // activation-tile ring.
-template <int NMAX>
+// MT: m-tiles per work item (1 or 2).  With two, one unit hands the issuer both m-tiles'
+// chunks (16 MMAs against one activation tile): the stage hand-off, not the MMAs, bounds
+// the pipeline at small group sizes, so a unit costs about the same with twice the work.
+// A stage holds MT x kUnit chunks; each accumulator buffer holds MT accumulators of NMAX
+// columns; ACCB: accumulator buffers (2: the epilogue overlaps the next item's MMAs).
+template <int NMAX, int MT = 1, int ACCB = 2>
 struct Plan {
   static constexpr int issuers = 1;
-  static constexpr int acc_bufs = 2;
-  static constexpr int stage_cols = 32 * kUnit;
-  static constexpr int stages_fit = (512 - acc_bufs * NMAX) / stage_cols;
+  static constexpr int acc_bufs = ACCB;
+  static constexpr int buf_cols = MT * NMAX;  // one accumulator buffer
+  static constexpr int stage_cols = 32 * kUnit * MT;
+  static constexpr int stages_fit = (512 - acc_bufs * buf_cols) / stage_cols;
   static constexpr int stages = stages_fit < kMaxStages ? stages_fit : kMaxStages;
   static constexpr int acc_col = stages * stage_cols;
 };
@@ -175,9 +186,9 @@ struct RunPos {
 
 // Consecutive CTAs take adjacent m-tiles of a group, which read the same activation tiles:
 // each CTA loads its own copy of them (the group's first reader brings them into L2).
-template <int BITS, bool DOWN, int NMAX>
+template <int BITS, bool DOWN, int NMAX, int MT, int ACCB>
 __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int item_bound) {
-  using PL = Plan<NMAX>;
+  using PL = Plan<NMAX, MT, ACCB>;
   using RG = Rings<NMAX, BITS>;
   constexpr int NI = PL::issuers;
   constexpr int AB = ATile<BITS>::bytes, RB = ATile<BITS>::row_bytes;
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   const int where = DOWN ? kKDown : kKGateUp;
   // ring geometry of this launch
   const int ra = a.ra, rb = a.rb;
-  const int a_run = ra * AB;                                  // bytes of a code run
+  const int a_run = MT * ra * AB;  // bytes of a code run: [m-tile][ra chunks]
   const int b_stride = (rb + (rb > 1 ? 1 : 0)) * NMAX * 128;  // run + the MMA's over-read
   const int SA = min(kMaxRuns, RG::a_ring / a_run), SB = min(kMaxRuns, RG::b_ring / b_stride);
   // TMEM stages in use.  A dequantiser set waits only on the ring runs of its own units, so
@@ -200,6 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
   // has landed, so the early pass cannot happen while the stages hold no more chunks than
   // either ring: kUnit * ST <= SA * ra and <= SB * rb.
   const int ST = min(PL::stages, min(SA * ra, SB * rb) / kUnit);
+  // Dequantiser sets in use.  A set waits on a stage's `done` barrier for the stage's
+  // previous unit, which another set may have taken; its own last unit on that stage is
+  // `sets` units back in the rotation, so with more sets than stages the stage can turn
+  // over twice between its waits and the parity test passes a lap early.  No more sets
+  // than stages, then (the others idle).
+  const int nsets = min(kDqSets, ST);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; s++) {
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       bool ok = true;
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
-        if (!tc_item<DOWN>(a, item, it)) break;
+        if (!tc_item<DOWN, MT>(a, item, it)) break;
         // the item's activation tiles are one contiguous range, read again by the group's
         // other m-tiles: start it towards L2 now, so that the ring's copies hit L2
         if (!isA)
@@ -258,8 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
           const uint32_t ph = pos.ph;
           if (!tc::mbar_wait_backoff(&empty[s], ph ^ 1, abort, lim, 64)) { ok = false; break; }
           if (isA) {
-            tc::mbar_arrive_expect_tx(&full[s], (uint32_t)a_run);
-            tc::bulk_g2s(aring + s * a_run, a_src<BITS, DOWN>(a, it, kc), a_run, &full[s]);
+            // one copy per m-tile of the item: [m-tile][ra chunks] in the run's stage
+            const int nmt = MT == 1 ? 1 : it.nmt;
+            tc::mbar_arrive_expect_tx(&full[s], (uint32_t)(nmt * ra * AB));
+            for (int m = 0; m < nmt; m++)
+              tc::bulk_g2s(aring + s * a_run + m * ra * AB, a_src<BITS, DOWN>(a, it, kc, m),
+                           ra * AB, &full[s]);
             MOE_TC_TRACE(0, run * R);
           } else {
             const uint32_t bytes = (uint32_t)R * it.rows8 * 128;
@@ -292,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
       bool ok = true, issued = false;
       Item it;
       for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
-        if (!tc_item<DOWN>(a, item, it)) break;
+        if (!tc_item<DOWN, MT>(a, item, it)) break;
         // accumulator buffer ab, used for the au-th time
         const int ab = n % PL::acc_bufs, au = n / PL::acc_bufs;
         int got = 1;
@@ -301,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         if (!ok) break;
         tc::fence_after_sync();
         const uint32_t idesc = tc::idesc_f16(0, it.Npad);  // fp16 x fp16 -> fp32
-        const uint32_t dcol = tbase + PL::acc_col + ab * NMAX;
+        // m-tile m of the item accumulates at dcol + m * NMAX
+        const uint32_t dcol = tbase + PL::acc_col + ab * PL::buf_cols;
         for (int ku = 0; ku < it.KC; ku += kUnit, tpos.next(ST)) {
           got = 1;
           if (leader) MOE_TC_TRACE(10, c);
@@ -315,13 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
           for (int j = 0; j < kUnit; j++, c++, bpos.next(rb, SB)) {
             const uint32_t bsm =
                 tc::smem_u32(bring + bpos.r.s * b_stride) + bpos.j * it.rows8 * 128;
+            // chunk j of m-tile m sits at stage column m * 32 * kUnit + j * 32
             const uint32_t acol = tbase + tpos.s * PL::stage_cols + j * 32;
             const bool last_of_run = bpos.j + 1 >= rb || ku + j + 1 >= it.KC;
             if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < 4; kk++)
-                tc::mma_ts(dcol, acol + kk * 8, tc::sdesc_sw128(bsm + kk * 32), idesc,
-                           ku + j + kk > 0);
+              for (int m = 0; m < MT; m++) {
+                if (MT == 1 || m < it.nmt) {
+#pragma unroll
+                  for (int kk = 0; kk < 4; kk++)
+                    tc::mma_ts(dcol + m * NMAX, acol + m * 32 * kUnit + kk * 8,
+                               tc::sdesc_sw128(bsm + kk * 32), idesc, ku + j + kk > 0);
+                }
+              }
               if (last_of_run) tc::mma_commit(&bars->b_empty[bpos.r.s]);  // release the stage
             }
           }
@@ -357,9 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     RunPos bpos;   // activation-tile run of chunk c
     bool ok = true;
     Item it;
-    for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x) {
-      if (!tc_item<DOWN>(a, item, it)) break;
-      for (int ku = 0; ku < it.KC; ku += kUnit, turn = turn + 1 == kDqSets ? 0 : turn + 1,
+    // sets beyond nsets idle
+    for (int item = blockIdx.x; ok && set < nsets && item < item_bound; item += gridDim.x) {
+      if (!tc_item<DOWN, MT>(a, item, it)) break;
+      for (int ku = 0; ku < it.KC; ku += kUnit, turn = turn + 1 == nsets ? 0 : turn + 1,
                tpos.next(ST)) {
         if (turn != set) {
 #pragma unroll
@@ -378,11 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
                                                              abort, lim, 32));
           if (!ok) break;
           MOE_TC_TRACE_R(2, c);
-          uint32_t v[32];
-          dequant_row<BITS>(aring + apos.r.s * a_run + apos.j * AB + r * RB, lane, v);
+#pragma unroll
+          for (int m = 0; m < MT; m++) {
+            if (MT == 1 || m < it.nmt) {  // row r of m-tile m: [m-tile][ra chunks] in the stage
+              uint32_t v[32];
+              dequant_row<BITS>(aring + apos.r.s * a_run + (m * ra + apos.j) * AB + r * RB,
+                                lane, v);
+              tc::tmem_st32(tbase + tlane + tpos.s * PL::stage_cols + m * 32 * kUnit + j * 32,
+                            v);
+            }
+          }
           __syncwarp();  // the warp's shared-memory reads are done: one arrival per warp
           if (lane == 0) tc::mbar_arrive(&bars->a_empty[apos.r.s]);
-          tc::tmem_st32(tbase + tlane + tpos.s * PL::stage_cols + j * 32, v);
           if (q == 0) {
             // the chunk's activation tile has landed: the published stage then stands for
             // both MMA operands (the tile's ring stage cannot be reused before this chunk's
@@ -407,12 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     const int q = warp & 3, r = 32 * q + lane;
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
     uint32_t d0 = tbase + tlane + PL::acc_col;  // + the item's buffer
-    // sum of the issuers' accumulators, 16 columns from c0
-    auto load_sum = [&](int c0, float (&v)[16]) {
+    // sum of the issuers' accumulators at column base d (+ issuer i's NMAX columns... one
+    // issuer here), 16 columns from c0
+    auto load_sum = [&](uint32_t d, int c0, float (&v)[16]) {
 #pragma unroll
       for (int i = 0; i < NI; i++) {
         uint32_t t[16];
-        tc::tmem_ld16(d0 + i * NMAX + c0, t);
+        tc::tmem_ld16(d + i * NMAX + c0, t);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int jj = 0; jj < 16; jj++) v[jj] = (i ? v[jj] : 0.f) + __uint_as_float(t[jj]);
@@ -422,18 +459,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     bool ok = true;
     Item it;
     for (int item = blockIdx.x; ok && item < item_bound; item += gridDim.x, n++) {
-      if (!tc_item<DOWN>(a, item, it)) break;
+      if (!tc_item<DOWN, MT>(a, item, it)) break;
       const int ab = n % PL::acc_bufs, au = n / PL::acc_bufs;
       ok = __all_sync(0xffffffffu,
                       tc::mbar_wait_backoff(&bars->acc_full[ab], au & 1, abort, lim, 256));
-      d0 = tbase + tlane + PL::acc_col + ab * NI * NMAX;
+      d0 = tbase + tlane + PL::acc_col + ab * PL::buf_cols;  // m-tile m at d0 + m * NMAX
       if (!ok) break;
       MOE_TC_TRACE_R(8, n);
       tc::fence_after_sync();
       const ExpertLayout &L = it.sh ? a.LS : a.LR;
       const int gn = it.g.n;
       if (!DOWN) {
-        const float s = ((const float *)(it.ebase + L.sgu_off))[it.mt * 128 + r];
         // 1 / the token's activation scale, per B row: loaded once per item into this warp's
         // slice of shared memory (no load waits behind the stores of the loop below)
         float *rsc = bars->escale[q];
@@ -443,47 +479,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
         __syncwarp();
         const int j = r >> 1;  // output index within the m-tile (64 outputs)
         const bool odd = r & 1;  // rows 2j (gate) and 2j + 1 (up) sit in adjacent lanes
-        uint8_t *hbase =
-            a.hg + (size_t)it.g.hrow0 * a.Imax * 2 + (size_t)it.mt * round8(gn) * 128;
         bool bad = false;
-        // tokens in pairs (i, i + 1): the gate lane computes h for token i, the up lane for
-        // token i + 1; one exchange gives each lane the other operand it needs
-        auto pair = [&](int i, float w0, float w1) {
-          const float other = __shfl_xor_sync(0xffffffffu, odd ? w0 : w1, 1);
-          const int tok = odd ? i + 1 : i;
-          const float g = odd ? other : w0, u = odd ? w1 : other;
-          if (tok < gn) {
-            const __half hv = __float2half_rn(silu_fast(g) * u);
-            bad |= __hisinf(hv) || __hisnan(hv);
-            *(__half *)(hbase + (size_t)tok * 128 + (((j >> 3) ^ (tok & 7)) << 4) + (j & 7) * 2) =
-                hv;
-          }
-        };
-        for (int c0 = 0; c0 < it.Npad; c0 += 16) {
-          float acc[16];
-          load_sum(c0, acc);
-          if (a.P == 1) {
+        const int nmt = MT == 1 ? 1 : it.nmt;
+        for (int m = 0; m < nmt; m++) {
+          const int mt = it.mt + m;
+          const float s = ((const float *)(it.ebase + L.sgu_off))[mt * 128 + r];
+          uint8_t *hbase =
+              a.hg + (size_t)it.g.hrow0 * a.Imax * 2 + (size_t)mt * round8(gn) * 128;
+          // tokens in pairs (i, i + 1): the gate lane computes h for token i, the up lane
+          // for token i + 1; one exchange gives each lane the other operand it needs
+          auto pair = [&](int i, float w0, float w1) {
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? w0 : w1, 1);
+            const int tok = odd ? i + 1 : i;
+            const float g = odd ? other : w0, u = odd ? w1 : other;
+            if (tok < gn) {
+              const __half hv = __float2half_rn(silu_fast(g) * u);
+              bad |= __hisinf(hv) || __hisnan(hv);
+              *(__half *)(hbase + (size_t)tok * 128 + (((j >> 3) ^ (tok & 7)) << 4) +
+                          (j & 7) * 2) = hv;
+            }
+          };
+          for (int c0 = 0; c0 < it.Npad; c0 += 16) {
+            float acc[16];
+            load_sum(d0 + m * NMAX, c0, acc);
+            if (a.P == 1) {
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 2)
-              pair(c0 + jj, acc[jj] * s * rsc[c0 + jj], acc[jj + 1] * s * rsc[c0 + jj + 1]);
-          } else {  // columns 2i, 2i + 1: the hi and lo pieces of token i
+              for (int jj = 0; jj < 16; jj += 2)
+                pair(c0 + jj, acc[jj] * s * rsc[c0 + jj], acc[jj + 1] * s * rsc[c0 + jj + 1]);
+            } else {  // columns 2i, 2i + 1: the hi and lo pieces of token i
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4)
-              pair((c0 + jj) >> 1, (acc[jj] + acc[jj + 1]) * s * rsc[c0 + jj],
-                   (acc[jj + 2] + acc[jj + 3]) * s * rsc[c0 + jj + 2]);
+              for (int jj = 0; jj < 16; jj += 4)
+                pair((c0 + jj) >> 1, (acc[jj] + acc[jj + 1]) * s * rsc[c0 + jj],
+                     (acc[jj + 2] + acc[jj + 3]) * s * rsc[c0 + jj + 2]);
+            }
           }
         }
         if (bad) record_status(a.ctrl, MOE_ERR_NUMERIC, where);
       } else {
-        const float s = ((const float *)(it.ebase + L.sd_off))[it.mt * 128 + r];
         const long yrow0 = it.sh ? (long)a.T * a.k + it.g.pos0 : (long)it.g.pos0;
-        float *ycol = a.y + yrow0 * a.H + it.mt * 128 + r;
-        for (int c0 = 0; c0 < it.Npad; c0 += 16) {
-          float acc[16];
-          load_sum(c0, acc);
+        const int nmt = MT == 1 ? 1 : it.nmt;
+        for (int m = 0; m < nmt; m++) {
+          const int mt = it.mt + m;
+          const float s = ((const float *)(it.ebase + L.sd_off))[mt * 128 + r];
+          float *ycol = a.y + yrow0 * a.H + mt * 128 + r;
+          for (int c0 = 0; c0 < it.Npad; c0 += 16) {
+            float acc[16];
+            load_sum(d0 + m * NMAX, c0, acc);
 #pragma unroll
-          for (int jj = 0; jj < 16; jj++)
-            if (c0 + jj < gn) ycol[(size_t)(c0 + jj) * a.H] = acc[jj] * s;
+            for (int jj = 0; jj < 16; jj++)
+              if (c0 + jj < gn) ycol[(size_t)(c0 + jj) * a.H] = acc[jj] * s;
+          }
         }
       }
       tc::fence_before_sync();
@@ -602,10 +647,10 @@ __global__ void __launch_bounds__(256) token_rows_kernel(TcArgs a, const void *x
     write_group_row_scales(a.groups[gi], a.E, a.k, a.P, a.perm, a.tscale, a.rscale, lane);
 }
 
-template <int BITS, bool DOWN, int NMAX>
+template <int BITS, bool DOWN, int NMAX, int MT, int ACCB>
 static int launch_tc(const TcArgs &a, int bound, int sms, cudaStream_t st) {
   constexpr size_t smem = tc_smem<NMAX, BITS>();
-  auto k = tc_expert_kernel<BITS, DOWN, NMAX>;
+  auto k = tc_expert_kernel<BITS, DOWN, NMAX, MT, ACCB>;
   set_dyn_smem((const void *)k, (int)smem);
   if (launch_pdl(k, dim3(bound < sms ? bound : sms), dim3(kThreads), smem, st, a, bound) !=
       cudaSuccess)
@@ -613,16 +658,29 @@ static int launch_tc(const TcArgs &a, int bound, int sms, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Launches of groups of up to 128 rows: one m-tile per work item, a double-buffered
+// accumulator and 4 stages (1 here).  Two m-tiles would leave TMEM room for a single
+// accumulator buffer and 2 stages, hence 2 dequantiser sets: slower at DSV3 T = 2048
+// (gate/up 1.40 vs 1.26 ms), while at <= 64 rows (T = 20..64) two m-tiles with a double
+// buffer take 12-20% less time than one.
+constexpr int kMt128 = 1;
+
 // NMAX: the smallest supported width >= the largest B row count of any group in the launch
+// (`bound`: an upper bound of the launch's items counted as single m-tiles)
 template <int BITS, bool DOWN>
 static int launch_tc_n(TcArgs a, int rows_max, int kc_gcd, int bound, int sms, cudaStream_t st) {
-  // chunks per copy: code runs of 4 chunks (16 KB at int4) where every K allows it;
-  // activation tiles in runs too when they are small (decode), else one chunk per copy
-  a.ra = kc_gcd % 4 == 0 ? 4 : (kc_gcd % 2 == 0 ? 2 : 1);
+  // chunks per copy: code runs of 4 chunks (16 KB at int4) where every K allows it, 2
+  // chunks of each of two m-tiles for two-m-tile items; activation tiles in runs too when
+  // they are small (decode), else one chunk per copy
+  const int ra1 = kc_gcd % 4 == 0 ? 4 : (kc_gcd % 2 == 0 ? 2 : 1);
+  const int ra2 = kc_gcd % 2 == 0 ? 2 : 1;
+  const bool two = rows_max <= 64 || kMt128 == 2;
+  a.ra = two ? ra2 : ra1;
   a.rb = rows_max <= 32 ? a.ra : 1;
-  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32>(a, bound, sms, st);
-  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64>(a, bound, sms, st);
-  return launch_tc<BITS, DOWN, 128>(a, bound, sms, st);
+  if (rows_max <= 32) return launch_tc<BITS, DOWN, 32, 2, 2>(a, bound, sms, st);
+  if (rows_max <= 64) return launch_tc<BITS, DOWN, 64, 2, 2>(a, bound, sms, st);
+  if (kMt128 == 2) return launch_tc<BITS, DOWN, 128, 2, 1>(a, bound, sms, st);
+  return launch_tc<BITS, DOWN, 128, 1, 2>(a, bound, sms, st);
 }
 
 static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }

@@ -247,6 +247,18 @@ def test_layer_decode_rows_without_gemv_router():
     check_layer(small("softmax", hidden=12416, inter=256), 16, seed=9)
 
 
+# An odd down m-tile count (H = 384: 3 m-tiles of 128 outputs; I is a multiple of 128, so
+# gate/up always has an even count): the tensor-core kernels take two m-tiles per work
+# item, so each group's last down item holds one.
+ODD_MT = gen.LayerSpec("odd_mtiles", hidden=384, inter=256, n_experts=8, top_k=2,
+                       router="softmax", n_shared=1, inter_shared=384)
+
+
+@pytest.mark.parametrize("T", [40, 300])
+def test_layer_odd_mtile_counts(T):
+    check_layer(ODD_MT, T)
+
+
 # A Mixtral-shaped small layer: few experts with a long down contraction, so the decode
 # down launch has few work items and splits each item's contraction (8 parts at T = 1 and
 # 2, 4 at T = 5 and 16; 4 with the shared expert), the combine adding the parts' y planes.

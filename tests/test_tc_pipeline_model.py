@@ -9,12 +9,16 @@ warps), lets bulk copies land in any order and MMA commits arrive in issue order
 the next runnable role at random.  It checks that
 
   - for every ring geometry the launcher can choose (int2/int4/int8 codes; 32-, 64- and
-    128-row launches; code runs of 1, 2 or 4 chunks), with the TMEM stages in use capped
-    as the kernel caps them (kUnit * stages <= chunks of either ring), no schedule
-    deadlocks and every wait passes on the phase it was meant for;
-  - without that cap, the int8 64-row launch (six stages of two chunks against a ring of
-    two 4-chunk code runs) has schedules in which a dequantiser set passes a code-ring wait
-    one lap early: the reason for the cap.
+    128-row launches with one or two m-tiles per work item; code runs of 1, 2 or 4
+    chunks), with the TMEM stages in use capped as the kernel caps them (kUnit * stages <=
+    chunks of either ring) and no more dequantiser sets than stages, no schedule deadlocks
+    and every wait passes on the phase it was meant for;
+  - without the stage cap, the int8 64-row launch (six stages of two chunks against a ring
+    of two 4-chunk code runs) has schedules in which a dequantiser set passes a code-ring
+    wait one lap early; with three sets on two stages, a set passes a stage's done wait a
+    lap early: the reasons for the two limits.
+The model's barrier arithmetic does not depend on the m-tiles per item (a unit's chunks
+carry both m-tiles' codes; the arrival counts are per chunk), only the geometry does.
 """
 import random
 
@@ -27,18 +31,30 @@ MAX_RUNS = 24
 MAX_STAGES = 16
 
 
-def geometry(bits, nmax, kc_gcd, capped=True):
-    """The launch's rings, as the kernel and its launcher size them."""
-    stages = min(MAX_STAGES, (512 - 2 * nmax) // (32 * K_UNIT))
+def launch_shape(nmax):
+    """(m-tiles per item, accumulator buffers) of a launch of groups of <= nmax rows."""
+    return (2, 2) if nmax <= 64 else (1, 2)
+
+
+def geometry(bits, nmax, kc_gcd, capped=True, mt=None, accb=None):
+    """The launch's rings, stages and dequantiser sets, as the kernel and its launcher
+    size them."""
+    if mt is None:
+        mt, accb = launch_shape(nmax)
+    stages = min(MAX_STAGES, (512 - accb * mt * nmax) // (32 * K_UNIT * mt))
     a_ring = 64 * 1024 if bits == 8 else 48 * 1024
     b_ring = SMEM_RINGS - a_ring
-    ra = 4 if kc_gcd % 4 == 0 else (2 if kc_gcd % 2 == 0 else 1)
+    if mt == 2:
+        ra = 2 if kc_gcd % 2 == 0 else 1
+    else:
+        ra = 4 if kc_gcd % 4 == 0 else (2 if kc_gcd % 2 == 0 else 1)
     rb = ra if nmax == 32 else 1
-    a_run = ra * 128 * 64 * bits // 8
+    a_run = mt * ra * 128 * 64 * bits // 8
     b_stride = (rb + (1 if rb > 1 else 0)) * nmax * 128
     sa, sb = min(MAX_RUNS, a_ring // a_run), min(MAX_RUNS, b_ring // b_stride)
     st = min(stages, min(sa * ra, sb * rb) // K_UNIT) if capped else stages
-    return dict(ST=st, SA=sa, ra=ra, SB=sb, rb=rb)
+    sets = min(N_SETS, st) if capped else N_SETS
+    return dict(ST=st, SA=sa, ra=ra, SB=sb, rb=rb, sets=sets)
 
 
 class Bar:
@@ -182,18 +198,19 @@ def run_schedule(seed, ST, SA, ra, SB, rb, items, sets=N_SETS):
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
-@pytest.mark.parametrize("nmax", [32, 64, 128])
+@pytest.mark.parametrize("nmax,mt,accb", [(32, 2, 2), (64, 2, 2), (128, 2, 1), (128, 1, 2)])
 @pytest.mark.parametrize("kc_gcd", [32, 6, 3])
-def test_capped_geometries_never_pass_early_or_deadlock(bits, nmax, kc_gcd):
-    geo = geometry(bits, nmax, kc_gcd)
+def test_capped_geometries_never_pass_early_or_deadlock(bits, nmax, mt, accb, kc_gcd):
+    geo = geometry(bits, nmax, kc_gcd, mt=mt, accb=accb)
     assert geo["ST"] >= 2 and K_UNIT * geo["ST"] <= min(geo["SA"] * geo["ra"], geo["SB"] * geo["rb"])
+    assert geo["sets"] <= geo["ST"]
     items = [kc_gcd * max(1, 12 // kc_gcd) * 2] * 3  # whole units, a few rings' worth
     for seed in range(12):
         assert run_schedule(seed, items=items, **geo) == "ok", (geo, seed)
 
 
 def test_uncapped_int8_64_row_launch_passes_a_code_wait_a_lap_early():
-    geo = geometry(8, 64, 32, capped=False)
+    geo = geometry(8, 64, 32, capped=False, mt=1, accb=2)
     assert geo["ST"] * K_UNIT > geo["SA"] * geo["ra"]  # 12 chunks of stages, 8 of code ring
     early = 0
     for seed in range(40):
@@ -202,7 +219,23 @@ def test_uncapped_int8_64_row_launch_passes_a_code_wait_a_lap_early():
         except EarlyPass:
             early += 1
     assert early > 0
-    capped = geometry(8, 64, 32)
+    capped = geometry(8, 64, 32, mt=1, accb=2)
     assert capped["ST"] == 4
     for seed in range(40):
         assert run_schedule(seed, items=[32] * 4, **capped) == "ok"
+
+
+def test_more_sets_than_stages_pass_a_done_wait_a_lap_early():
+    # the 64-row launch (two m-tiles per item) has two stages: three sets would each come
+    # back to a stage only every sixth unit, after it turned over twice
+    geo = geometry(4, 64, 32)
+    assert geo["ST"] == 2 and geo["sets"] == 2
+    early = 0
+    for seed in range(20):
+        try:
+            run_schedule(seed, items=[96] * 2, **dict(geo, sets=3))
+        except EarlyPass:
+            early += 1
+    assert early > 0
+    for seed in range(20):
+        assert run_schedule(seed, items=[96] * 2, **geo) == "ok"
