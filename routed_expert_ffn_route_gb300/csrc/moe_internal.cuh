@@ -167,7 +167,13 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   W.tc = use_tc(c);
   W.pieces = pieces;
   int gn_min = W.tc ? kTcMaxRows / 2 : choose_group_n(c, T);
-  W.group_n = W.tc ? kTcMaxRows / pieces : gn_min;
+  // Tensor-core groups of at most 128 B rows, or 64 when the batch gives an expert few
+  // tokens on average (T k <= 16 E): launches of <= 64-row groups take two m-tiles per work
+  // item, which saves more than the few large groups lose by reading their codes twice
+  // (DSV3 T = 128 / 256: gate/up + down 987 -> 858, 1110 -> 985 us; at T = 1024 the cap
+  // costs 20%).  The work list is sized for 64-row groups either way.
+  const int gcap = (long)T * k <= 16L * c.n_experts ? kTcMaxRows / 2 : kTcMaxRows;
+  W.group_n = W.tc ? gcap / pieces : gn_min;
   W.rows = T * k + (c.n_shared ? T : 0);
   W.e0 = 0;
   W.e1 = c.n_experts;

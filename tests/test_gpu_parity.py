@@ -310,9 +310,11 @@ def test_layer_deterministic_and_T0_noop():
 # full-size layers (the benchmark's shapes): every token up to T = 64; at prefill sizes
 # every token of the three most-loaded experts (their groups cover every m-tile of the
 # tensor-core kernel, and an expert with more than 128 tokens forms two groups) plus 32
-# spread tokens (one in every group of the shared expert)
+# spread tokens (one in every group of the shared expert).  DSV3 at T = 256 gives an
+# expert 8 tokens on average: groups of at most 64 rows, two m-tiles per work item.
 @pytest.mark.parametrize("name,T,sample", [("mixtral", 1, None), ("dsv3", 1, None),
-                                           ("dsv3", 16, None), ("dsv3", 2048, "prefill"),
+                                           ("dsv3", 16, None), ("dsv3", 256, "prefill"),
+                                           ("dsv3", 2048, "prefill"),
                                            ("dsv3_int2", 1, None), ("dsv3_int8", 4, None),
                                            ("dsv3_int8", 64, None), ("mixtral", 512, "prefill")])
 def test_layer_full_size(name, T, sample):
