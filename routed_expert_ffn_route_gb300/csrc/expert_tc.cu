@@ -679,8 +679,8 @@ static int launch_tc_n(TcArgs a, int rows_max, int kc_gcd, int bound, int sms, c
   a.rb = rows_max <= 32 ? a.ra : 1;
   if (rows_max <= 32) return launch_tc<BITS, DOWN, 32, 2, 2>(a, bound, sms, st);
   if (rows_max <= 64) return launch_tc<BITS, DOWN, 64, 2, 2>(a, bound, sms, st);
-  if (kMt128 == 2) return launch_tc<BITS, DOWN, 128, 2, 1>(a, bound, sms, st);
-  return launch_tc<BITS, DOWN, 128, 1, 2>(a, bound, sms, st);
+  if constexpr (kMt128 == 2) return launch_tc<BITS, DOWN, 128, 2, 1>(a, bound, sms, st);
+  else return launch_tc<BITS, DOWN, 128, 1, 2>(a, bound, sms, st);
 }
 
 static int gcd_i(int x, int y) { return y ? gcd_i(y, x % y) : x; }
