@@ -443,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(TcArgs a, int it
     const int q = warp & 3, r = 32 * q + lane;
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
     uint32_t d0 = tbase + tlane + PL::acc_col;  // + the item's buffer
-    // sum of the issuers' accumulators at column base d (+ issuer i's NMAX columns... one
-    // issuer here), 16 columns from c0
+    // 16 accumulator columns from c0 of the accumulator at column d (summed over the
+    // issuers' copies, NMAX columns apart; one issuer here)
     auto load_sum = [&](uint32_t d, int c0, float (&v)[16]) {
 #pragma unroll
       for (int i = 0; i < NI; i++) {
