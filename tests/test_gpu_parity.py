@@ -260,8 +260,9 @@ def test_layer_odd_mtile_counts(T):
 
 
 # A Mixtral-shaped small layer: few experts with a long down contraction, so the decode
-# down launch has few work items and splits each item's contraction (8 parts at T = 1 and
-# 2, 4 at T = 5 and 16; 4 with the shared expert), the combine adding the parts' y planes.
+# down launch has few work items and splits each item's contraction (8 parts; 4 with the
+# shared expert, whose contraction has fewer code runs), the combine adding the parts' y
+# planes.
 MIX_SPLIT = gen.LayerSpec("mix_split", hidden=1024, inter=2048, n_experts=8, top_k=2,
                           router="softmax")
 
