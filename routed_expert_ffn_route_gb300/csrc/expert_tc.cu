@@ -49,8 +49,8 @@ namespace moe {
 
 // Pipeline tracing for development builds (-DMOE_TRACE): the SM clock at each hand-off of
 // the first kTraceChunks chunks of CTA 0, one row of kTraceChunks per event.
-constexpr int kTraceChunks = 256;
 #ifdef MOE_TRACE
+constexpr int kTraceChunks = 256;
 #define MOE_TC_TRACE(ev, c)                                               \
   do {                                                                    \
     if (blockIdx.x == 0 && a.trace && (c) < kTraceChunks)                 \
