@@ -33,7 +33,7 @@ MAX_STAGES = 16
 
 def launch_shape(nmax):
     """(m-tiles per item, accumulator buffers) of a launch of groups of <= nmax rows."""
-    return (2, 2) if nmax <= 64 else (1, 2)
+    return {32: (2, 2), 64: (2, 1)}.get(nmax, (1, 2))
 
 
 def geometry(bits, nmax, kc_gcd, capped=True, mt=None, accb=None):
@@ -198,7 +198,8 @@ def run_schedule(seed, ST, SA, ra, SB, rb, items, sets=N_SETS):
 
 
 @pytest.mark.parametrize("bits", [2, 4, 8])
-@pytest.mark.parametrize("nmax,mt,accb", [(32, 2, 2), (64, 2, 2), (128, 2, 1), (128, 1, 2)])
+@pytest.mark.parametrize("nmax,mt,accb", [(32, 2, 2), (64, 2, 1), (64, 2, 2), (128, 2, 1),
+                                          (128, 1, 2)])
 @pytest.mark.parametrize("kc_gcd", [32, 6, 3])
 def test_capped_geometries_never_pass_early_or_deadlock(bits, nmax, mt, accb, kc_gcd):
     geo = geometry(bits, nmax, kc_gcd, mt=mt, accb=accb)
@@ -226,9 +227,10 @@ def test_uncapped_int8_64_row_launch_passes_a_code_wait_a_lap_early():
 
 
 def test_more_sets_than_stages_pass_a_done_wait_a_lap_early():
-    # the 64-row launch (two m-tiles per item) has two stages: three sets would each come
-    # back to a stage only every sixth unit, after it turned over twice
-    geo = geometry(4, 64, 32)
+    # a 64-row launch with two m-tiles per item and two accumulator buffers has two stages:
+    # three sets would each come back to a stage only every sixth unit, after it turned
+    # over twice
+    geo = geometry(4, 64, 32, mt=2, accb=2)
     assert geo["ST"] == 2 and geo["sets"] == 2
     early = 0
     for seed in range(20):
