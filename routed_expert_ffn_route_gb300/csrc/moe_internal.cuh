@@ -170,7 +170,7 @@ static inline WsLayout ws_layout(const moe_layer_config &c, int T, int pieces = 
   // Tensor-core groups of at most 128 B rows, or 64 when the batch gives an expert few
   // tokens on average (T k <= 16 E): launches of <= 64-row groups take two m-tiles per work
   // item, which saves more than the few large groups lose by reading their codes twice
-  // (DSV3 T = 128 / 256: gate/up + down 987 -> 858, 1110 -> 985 us; at T = 1024 the cap
+  // (DSV3 T = 128 / 256: gate/up + down 987 -> 812, 1110 -> 949 us; at T = 1024 the cap
   // costs 20%).  The work list is sized for 64-row groups either way.
   const int gcap = (long)T * k <= 16L * c.n_experts ? kTcMaxRows / 2 : kTcMaxRows;
   W.group_n = W.tc ? gcap / pieces : gn_min;
