@@ -144,9 +144,11 @@ MIX_SPLIT = gen.LayerSpec("mix_split", hidden=1024, inter=2048, n_experts=8, top
                           router="softmax")
 
 
-@pytest.mark.parametrize("spec", [gen.spec("dsv3"), gen.spec("tiny"), MIX_SPLIT,
+@pytest.mark.parametrize("spec", [gen.spec("dsv3"), gen.spec("tiny"), gen.spec("dsv3_int8"),
+                                  gen.spec("dsv3_int2"), gen.spec("mixtral"), MIX_SPLIT,
                                   MIX_SPLIT.replace(n_shared=1, inter_shared=1024)],
-                         ids=["dsv3", "tiny", "mix_split", "mix_split_shared"])
+                         ids=["dsv3", "tiny", "dsv3_int8", "dsv3_int2", "mixtral", "mix_split",
+                              "mix_split_shared"])
 def test_workspace_never_shrinks_as_tokens_grow(spec, L):
     """A workspace sized for T tokens serves every call of T' <= T tokens, so the size is
     monotone in T (the split down launch's extra y planes are largest at small T)."""
